@@ -1,0 +1,146 @@
+/*
+ * flce.h — C ABI of the GB300 (sm_103a) fused linear cross-entropy library.
+ *
+ * Fused linear cross-entropy (FLCE) computes the language-model-head loss
+ *
+ *     z_iv  = h_i . w_v                      (logits Z = H W^T, never stored)
+ *     lse_i = log sum_v exp(z_iv)
+ *     loss  = sum_{i valid} (lse_i - z_{i,y_i}) / n      (reduction "mean")
+ *
+ * and its gradients
+ *
+ *     G     = (softmax(Z) - onehot(y)) * grad_scale / n   (rows of ignored tokens are 0)
+ *     dH    = G W          dW = G^T H
+ *
+ * without writing the [N, V] logits to device memory.
+ *
+ * Sources: "Liger Kernel: Fused Triton Kernels for LLM Training", section "The
+ * Architecture" (1. Fused Linear Cross-Entropy with Online LogSumExp: the
+ * stable LSE, target-logit extraction, only the loss and per-token normalisers
+ * kept; 2. In-Kernel Gradient Computation During the Backward Pass: softmax minus
+ * one-hot, dL/dH = (dL/dZ) W, dL/dW = (dL/dZ)^T H, tile logits recomputed from the
+ * saved LSE), with the 1/N mean factor of the same page's section
+ * "Implementation: Simulating Fused Linear Cross-Entropy in Python"; GPU MODE
+ * lecture 28 notes, cross-entropy section: the fused loss takes hidden states
+ * (B*S, hidden), the LM-head weight (vocab, hidden) and labels, and replaces
+ * PyTorch's cross entropy with reduction="mean".
+ *
+ * Conventions for every entry point
+ *   - Matrices are dense, row-major, device memory: H is bf16 [N, D], W is bf16
+ *     [V, D], labels are int32 [N]. bf16 values are passed as their uint16_t bit
+ *     patterns. Every device pointer must be 16-byte aligned and D % 8 == 0 (the
+ *     tensor-memory-access engine needs 16-byte row strides).
+ *   - Ownership: the caller allocates and frees every buffer, the workspace
+ *     included. The library allocates no device memory and keeps no pointer after
+ *     a call returns (it caches only host-side descriptors keyed by pointer and
+ *     shape).
+ *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and return before it finishes. Outputs are
+ *     overwritten, never accumulated into.
+ *   - Host-side errors are returned immediately and nothing is enqueued.
+ *     Data-dependent errors found on the device (a label out of range, a wait
+ *     that ran out of time) are written to the optional device word `status`;
+ *     read it with flce_check_status(). When a device error is reported the
+ *     outputs of that call are undefined, but no memory outside the given
+ *     buffers is touched.
+ *   - Labels equal to ignore_index contribute neither to the loss nor to the
+ *     gradients and are not counted in n. If every label is ignored the loss
+ *     and the gradients are 0 (not NaN); lse is still written for every token.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (host) and device status words. */
+enum {
+  FLCE_OK = 0,
+  FLCE_ERR_NULL = 1,        /* a required pointer is NULL */
+  FLCE_ERR_SHAPE = 2,       /* N, D or V < 1, or too large for int32 indexing */
+  FLCE_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned, or D % 8 != 0 */
+  FLCE_ERR_WORKSPACE = 4,   /* workspace smaller than flce_workspace_size() */
+  FLCE_ERR_OPTION = 5,      /* an option is out of its range */
+  FLCE_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+  FLCE_ERR_DEVICE = 7,      /* the current device is not an sm_103 GPU */
+  FLCE_ERR_LABEL_RANGE = 8, /* device: a label is outside [0, V) and is not ignore_index */
+  FLCE_ERR_TIMEOUT = 9      /* device: a pipeline wait exceeded timeout_ns */
+};
+
+enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 };
+enum { FLCE_DTYPE_F32 = 0, FLCE_DTYPE_BF16 = 1 };
+
+typedef struct flce_options {
+  int32_t ignore_index; /* label value that marks an ignored token; default -100 */
+  int32_t reduction;    /* FLCE_REDUCTION_MEAN (default) or FLCE_REDUCTION_SUM */
+  float grad_scale;     /* upstream dL/dloss multiplying G; default 1 */
+  float normalizer;     /* > 0: mean divides by this instead of the device-counted n
+                           (a global token count for data-parallel callers); default 0 */
+  int32_t dw_dtype;     /* dW element type: FLCE_DTYPE_F32 (default) or FLCE_DTYPE_BF16 */
+  int32_t v_splits;     /* forward: vocabulary ranges per token block; 0 = planned */
+  int64_t n_block;      /* backward: tokens per block (multiple of 128); 0 = planned */
+  int64_t v_chunk;      /* backward: vocabulary ids per G chunk (multiple of 256); 0 = planned */
+  int64_t timeout_ns;   /* limit of every device-side pipeline wait; 0 = 2 s */
+} flce_options;
+
+/* Fill *opt with the defaults listed above. */
+void flce_default_options(flce_options* opt);
+
+/*
+ * Bytes of device workspace that flce_forward_backward and flce_forward need for
+ * this problem and these options (opt may be NULL for the defaults). The
+ * workspace holds the per-(token, vocabulary range) partial max/sum-exp pairs,
+ * the target logits, one bf16 chunk of G ([n_block, v_chunk]) and, when the
+ * vocabulary spans several chunks, an fp32 [n_block, D] dH accumulator (plus an
+ * fp32 [V, D] dW accumulator only for bf16 dW with several token blocks). It is
+ * the whole extra device memory of a call and is far below the N*V*4 bytes of
+ * fp32 logits. Returns FLCE_OK and writes *bytes, or an error code.
+ */
+int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt, size_t* bytes);
+
+/*
+ * Loss, per-token LSE and both gradients in one call.
+ *   H       bf16 [N, D]   hidden states (input)
+ *   W       bf16 [V, D]   LM-head weight (input)
+ *   labels  int32 [N]     target ids in [0, V) or ignore_index (input)
+ *   loss    fp32 [1]      scalar loss (output, required)
+ *   lse     fp32 [N]      log-sum-exp of each token's logits (output, may be NULL)
+ *   dH      bf16 [N, D]   dL/dH (output, may be NULL to skip the dH product)
+ *   dW      [V, D]        dL/dW, fp32 or bf16 per opt->dw_dtype (output, may be NULL)
+ *   workspace, ws_bytes   device scratch of at least flce_workspace_size() bytes
+ *   status  int32 [1]     device status word (may be NULL); set to FLCE_OK at the
+ *                         start of the call and to a device error code on failure
+ *   stream  cudaStream_t
+ */
+int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N,
+                          int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
+                          uint16_t* dH, void* dW, void* workspace, size_t ws_bytes,
+                          int32_t* status, void* stream);
+
+/*
+ * Forward only: the loss and (optionally) lse, without any gradient work. Same
+ * arguments and rules as flce_forward_backward.
+ */
+int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
+                 int64_t V, const flce_options* opt, float* loss, float* lse, void* workspace,
+                 size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Synchronise `stream`, read the device status word and return it (FLCE_OK, or
+ * the first device error a call recorded). Returns FLCE_ERR_CUDA if the stream
+ * reports a CUDA error. status == NULL returns FLCE_OK after the synchronisation.
+ */
+int flce_check_status(const int32_t* status, void* stream);
+
+/* Static English text for a return code. */
+const char* flce_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

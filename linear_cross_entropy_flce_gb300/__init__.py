@@ -1,0 +1,18 @@
+"""Fused linear cross-entropy for GB300 (sm_103a).
+
+The loss of a language-model head, mean over non-ignored tokens of
+logsumexp(h_i W^T) - h_i . w_{y_i}, and its gradients dH and dW, computed by
+hand-written tcgen05/TMA CUDA kernels without writing the [N, V] logits to
+device memory. The C ABI is include/flce.h; this package is its Python binding.
+"""
+from ._binding import (FLCE_ERR_ALIGN, FLCE_ERR_CUDA, FLCE_ERR_DEVICE, FLCE_ERR_LABEL_RANGE,
+                       FLCE_ERR_NULL, FLCE_ERR_OPTION, FLCE_ERR_SHAPE, FLCE_ERR_TIMEOUT,
+                       FLCE_ERR_WORKSPACE, FLCE_OK, FLCEError, LIB_PATH, Options, Result,
+                       check_status, forward, forward_backward, lib, make_options,
+                       status_string, workspace_size)
+
+__all__ = ["FLCE_ERR_ALIGN", "FLCE_ERR_CUDA", "FLCE_ERR_DEVICE", "FLCE_ERR_LABEL_RANGE",
+           "FLCE_ERR_NULL", "FLCE_ERR_OPTION", "FLCE_ERR_SHAPE", "FLCE_ERR_TIMEOUT",
+           "FLCE_ERR_WORKSPACE", "FLCE_OK", "FLCEError", "LIB_PATH", "Options", "Result",
+           "check_status", "forward", "forward_backward", "lib", "make_options",
+           "status_string", "workspace_size"]

@@ -1,0 +1,219 @@
+"""ctypes binding of libflce.so (include/flce.h): argument marshalling only.
+
+Every computation happens in the library's CUDA kernels. PyTorch is used here
+only for device memory, streams and tensor metadata. If the library has not
+been built, importing this module raises ImportError: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libflce.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "flce.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+        "(fused linear cross-entropy has no CPU or PyTorch fallback)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+FLCE_OK = 0
+FLCE_ERR_NULL = 1
+FLCE_ERR_SHAPE = 2
+FLCE_ERR_ALIGN = 3
+FLCE_ERR_WORKSPACE = 4
+FLCE_ERR_OPTION = 5
+FLCE_ERR_CUDA = 6
+FLCE_ERR_DEVICE = 7
+FLCE_ERR_LABEL_RANGE = 8
+FLCE_ERR_TIMEOUT = 9
+
+REDUCTIONS = {"mean": 0, "sum": 1}
+DW_DTYPES = {"float32": 0, "bfloat16": 1}
+
+
+class Options(ctypes.Structure):
+    _fields_ = [
+        ("ignore_index", ctypes.c_int32),
+        ("reduction", ctypes.c_int32),
+        ("grad_scale", ctypes.c_float),
+        ("normalizer", ctypes.c_float),
+        ("dw_dtype", ctypes.c_int32),
+        ("v_splits", ctypes.c_int32),
+        ("n_block", ctypes.c_int64),
+        ("v_chunk", ctypes.c_int64),
+        ("timeout_ns", ctypes.c_int64),
+    ]
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+lib.flce_default_options.argtypes = [ctypes.POINTER(Options)]
+lib.flce_default_options.restype = None
+lib.flce_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options),
+                                    ctypes.POINTER(ctypes.c_size_t)]
+lib.flce_workspace_size.restype = ctypes.c_int
+lib.flce_forward_backward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Options),
+                                      _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+lib.flce_forward_backward.restype = ctypes.c_int
+lib.flce_forward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Options),
+                             _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+lib.flce_forward.restype = ctypes.c_int
+lib.flce_check_status.argtypes = [_vp, _vp]
+lib.flce_check_status.restype = ctypes.c_int
+lib.flce_status_string.argtypes = [ctypes.c_int]
+lib.flce_status_string.restype = ctypes.c_char_p
+
+
+class FLCEError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: flce error {code}: {status_string(code)}")
+
+
+def status_string(code: int) -> str:
+    return lib.flce_status_string(int(code)).decode()
+
+
+def make_options(*, ignore_index: int = -100, reduction: str = "mean", grad_scale: float = 1.0,
+                 normalizer: float = 0.0, dw_dtype: str = "float32", v_splits: int = 0,
+                 n_block: int = 0, v_chunk: int = 0, timeout_ns: int = 0) -> Options:
+    o = Options()
+    lib.flce_default_options(ctypes.byref(o))
+    o.ignore_index = int(ignore_index)
+    o.reduction = REDUCTIONS[reduction]
+    o.grad_scale = float(grad_scale)
+    o.normalizer = float(normalizer)
+    o.dw_dtype = DW_DTYPES[dw_dtype]
+    o.v_splits = int(v_splits)
+    o.n_block = int(n_block)
+    o.v_chunk = int(v_chunk)
+    o.timeout_ns = int(timeout_ns)
+    return o
+
+
+def workspace_size(N: int, D: int, V: int, opts: Optional[Options] = None) -> int:
+    out = ctypes.c_size_t(0)
+    rc = lib.flce_workspace_size(N, D, V, ctypes.byref(opts) if opts is not None else None,
+                                 ctypes.byref(out))
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_workspace_size")
+    return int(out.value)
+
+
+@dataclasses.dataclass
+class Result:
+    loss: "object"           # torch float32 [1]
+    lse: "object"            # torch float32 [N]
+    dH: "object" = None      # torch bfloat16 [N, D] or None
+    dW: "object" = None      # torch float32/bfloat16 [V, D] or None
+    status: "object" = None  # torch int32 [1] (device status word)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _check_inputs(H, W, labels):
+    import torch
+    if not (H.is_cuda and W.is_cuda and labels.is_cuda):
+        raise ValueError("H, W and labels must be CUDA tensors")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    if H.dim() != 2 or W.dim() != 2 or labels.dim() != 1:
+        raise ValueError("H must be [N, D], W [V, D], labels [N]")
+    if not (H.is_contiguous() and W.is_contiguous() and labels.is_contiguous()):
+        raise ValueError("H, W and labels must be contiguous")
+    N, D = H.shape
+    V, D2 = W.shape
+    if D2 != D or labels.shape[0] != N:
+        raise ValueError("shape mismatch between H, W and labels")
+    return N, D, V
+
+
+def forward_backward(H, W, labels, *, need_dh: bool = True, need_dw: bool = True,
+                     out: Optional[dict] = None, workspace=None, status=None, stream=None,
+                     **options) -> Result:
+    """Loss, lse, dH and dW of fused linear cross-entropy via flce_forward_backward.
+
+    options: ignore_index, reduction ("mean"/"sum"), grad_scale, normalizer,
+    dw_dtype ("float32"/"bfloat16"), v_splits, n_block, v_chunk, timeout_ns.
+    `out` may hold preallocated "loss", "lse", "dH", "dW" tensors.
+    """
+    import torch
+    N, D, V = _check_inputs(H, W, labels)
+    opts = make_options(**options)
+    dev = H.device
+    out = dict(out or {})
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = out.get("dH")
+    if dH is None and need_dh:
+        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = out.get("dW")
+    if dW is None and need_dw:
+        dt = torch.float32 if options.get("dw_dtype", "float32") == "float32" else torch.bfloat16
+        dW = torch.empty(V, D, dtype=dt, device=dev)
+    ws_bytes = workspace_size(N, D, V, opts)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_forward_backward(_ptr(H), _ptr(W), _ptr(labels), N, D, V, ctypes.byref(opts),
+                                   _ptr(loss), _ptr(lse), _ptr(dH) if need_dh else None,
+                                   _ptr(dW) if need_dw else None, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(status),
+                                   stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_backward")
+    return Result(loss, lse, dH if need_dh else None, dW if need_dw else None, status)
+
+
+def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=None,
+            stream=None, **options) -> Result:
+    """Loss and lse only, via flce_forward."""
+    import torch
+    N, D, V = _check_inputs(H, W, labels)
+    opts = make_options(**options)
+    dev = H.device
+    out = dict(out or {})
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    ws_bytes = workspace_size(N, D, V, opts)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_forward(_ptr(H), _ptr(W), _ptr(labels), N, D, V, ctypes.byref(opts),
+                          _ptr(loss), _ptr(lse), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward")
+    return Result(loss, lse, None, None, status)
+
+
+def check_status(status, stream=None) -> int:
+    """Synchronise the stream and return the device status word (0 = ok)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(status.device).cuda_stream
+    return int(lib.flce_check_status(_ptr(status), stream))

@@ -1,0 +1,502 @@
+// C ABI of the fused linear cross-entropy library (declared in include/flce.h):
+// argument checks, the workspace plan, tensor-map encoding and the stream-ordered
+// launch sequence.
+//
+// Launch sequence of flce_forward_backward (all on the caller's stream):
+//   1. LSE GEMM   Z = H W^T, online max/sum-exp per (token block, vocabulary
+//                 range) and the target logit      ("Liger Kernel: Fused Triton
+//                 Kernels for LLM Training", The Architecture, 1.)
+//   2. merge      per-token lse and NLL from the partials
+//   3. reduce     n_valid, label check, loss, gradient scale (one block, fixed order)
+//   4. for each token block b, for each vocabulary chunk c:
+//        GRAD GEMM  recompute Z_bc, write G_bc = (softmax - onehot) * scale in bf16
+//        dW GEMM    dW_c  (+)= G_bc^T H_b   (fixed order over token blocks)
+//        dH GEMM    dH_b  (+)= G_bc W_c     (fp32 accumulator; the last chunk
+//                   rounds to bf16)              (same page, 2.)
+// Nothing of size N x V is ever written: the largest buffer is one G chunk.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/flce.h"
+#include "flce_internal.h"
+
+namespace flce {
+namespace {
+
+constexpr int64_t kDefaultTimeoutNs = 2000000000LL;
+constexpr size_t kGChunkCapBytes = size_t(256) << 20;  // planned bf16 G chunk
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct DeviceInfo {
+  bool init = false;
+  int status = FLCE_OK;
+  int sms = 0;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, count = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return FLCE_ERR_CUDA;
+    }
+    d.status = (major == 10 && minor == 3) ? FLCE_OK : FLCE_ERR_DEVICE;
+    d.sms = count;
+    d.init = true;
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  });
+  return fn;
+}
+
+// bf16 matrix [outer][inner] (inner contiguous, row stride ld elements), read in
+// boxes of box_inner x box_outer with 128-byte swizzle; out-of-range elements
+// read as zero.
+bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                 uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int64_t N = 0, D = 0, V = 0;
+  int m_blocks = 0;   // ceil(N / BM)
+  int v_tiles = 0;    // ceil(V / BN)
+  int splits = 0;     // forward vocabulary ranges per token block
+  int64_t n_block = 0, v_chunk = 0;
+  int n_nblocks = 0, n_chunks = 0;
+  bool need_dh_acc = false, need_dw_acc = false;
+  size_t off_part = 0, off_zt = 0, off_nll = 0, off_lse = 0, off_scal = 0, off_g = 0,
+         off_dhacc = 0, off_dwacc = 0, total = 0;
+};
+
+int choose_splits(int m_blocks, int v_tiles, int sms) {
+  // Minimise (waves of units) x (tiles per unit); ties go to fewer splits.
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  const int max_s = std::min(v_tiles, 128);
+  for (int s = 1; s <= max_s; ++s) {
+    const int64_t waves = ceil_div(static_cast<int64_t>(m_blocks) * s, sms);
+    const int64_t cost = waves * ceil_div(v_tiles, s);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, Plan* P) {
+  Plan p;
+  p.N = N;
+  p.D = D;
+  p.V = V;
+  p.m_blocks = static_cast<int>(ceil_div(N, BM));
+  p.v_tiles = static_cast<int>(ceil_div(V, BN));
+  if (o.v_splits < 0 || o.v_splits > p.v_tiles) return FLCE_ERR_OPTION;
+  p.splits = o.v_splits > 0 ? o.v_splits : choose_splits(p.m_blocks, p.v_tiles, sms);
+
+  const int64_t v_round = ceil_div(V, BN) * BN;
+  if (o.v_chunk < 0 || o.n_block < 0) return FLCE_ERR_OPTION;
+  if (o.v_chunk > 0 && o.v_chunk % BN != 0) return FLCE_ERR_OPTION;
+  if (o.n_block > 0 && o.n_block % BM != 0) return FLCE_ERR_OPTION;
+  // Planned G chunk: at most kGChunkCapBytes and at most an eighth of the
+  // vocabulary (but never below 2048 ids), balanced so that the chunks have
+  // nearly equal length. All tokens form one block unless that would push the
+  // chunk below 2048 ids.
+  int64_t cv = o.v_chunk, nb = o.n_block;
+  auto cv_for_rows = [&](int64_t rows) {
+    const int64_t r = ceil_div(rows, BM) * BM;
+    int64_t m = std::min<int64_t>(16384, static_cast<int64_t>(kGChunkCapBytes / (2 * r)));
+    m = std::min<int64_t>(m, std::max<int64_t>(2048, V / 8));
+    m = std::max<int64_t>(BN, m / BN * BN);
+    const int64_t chunks = ceil_div(V, m);
+    return ceil_div(ceil_div(V, chunks), BN) * BN;
+  };
+  auto nb_for_cv = [&](int64_t c) {
+    const int64_t r = static_cast<int64_t>(kGChunkCapBytes / (2 * c)) / BM * BM;
+    return std::max<int64_t>(BM, r);
+  };
+  if (cv == 0 && nb == 0) {
+    const int64_t r = ceil_div(N, BM) * BM;
+    if (static_cast<int64_t>(kGChunkCapBytes / (2 * r)) >= 2048) {
+      cv = cv_for_rows(N);
+      nb = N;
+    } else {
+      cv = 2048;
+      nb = nb_for_cv(cv);
+    }
+  } else if (cv == 0) {
+    cv = cv_for_rows(std::min(nb, N));
+  } else if (nb == 0) {
+    nb = nb_for_cv(cv);
+  }
+  cv = std::min(cv, v_round);
+  nb = std::min(nb, N);
+  p.v_chunk = cv;
+  p.n_block = nb;
+  p.n_chunks = static_cast<int>(ceil_div(V, cv));
+  p.n_nblocks = static_cast<int>(ceil_div(N, nb));
+  p.need_dh_acc = p.n_chunks > 1;
+  p.need_dw_acc = (o.dw_dtype == FLCE_DTYPE_BF16) && p.n_nblocks > 1;
+
+  const int64_t rows_b = ceil_div(nb, BM) * BM;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  p.off_part = take(static_cast<size_t>(p.splits) * p.m_blocks * BM * sizeof(float2));
+  p.off_zt = take(static_cast<size_t>(N) * 4);
+  p.off_nll = take(static_cast<size_t>(N) * 4);
+  p.off_lse = take(static_cast<size_t>(N) * 4);
+  p.off_scal = take(256);
+  p.off_g = take(static_cast<size_t>(rows_b) * cv * 2);
+  p.off_dhacc = p.need_dh_acc ? take(static_cast<size_t>(rows_b) * D * 4) : off;
+  p.off_dwacc = p.need_dw_acc ? take(static_cast<size_t>(V) * D * 4) : off;
+  p.total = off;
+  *P = p;
+  return FLCE_OK;
+}
+
+int check_options(const flce_options& o) {
+  if (o.reduction != FLCE_REDUCTION_MEAN && o.reduction != FLCE_REDUCTION_SUM)
+    return FLCE_ERR_OPTION;
+  if (o.dw_dtype != FLCE_DTYPE_F32 && o.dw_dtype != FLCE_DTYPE_BF16) return FLCE_ERR_OPTION;
+  if (!(o.normalizer >= 0.f) || !(o.grad_scale == o.grad_scale)) return FLCE_ERR_OPTION;
+  if (o.timeout_ns < 0) return FLCE_ERR_OPTION;
+  return FLCE_OK;
+}
+
+int check_shape(int64_t N, int64_t D, int64_t V) {
+  if (N < 1 || D < 1 || V < 1) return FLCE_ERR_SHAPE;
+  // int32 coordinates and indices inside the kernels
+  if (N > (int64_t(1) << 30) || V > (int64_t(1) << 30) || D > (int64_t(1) << 20))
+    return FLCE_ERR_SHAPE;
+  if (D % 8 != 0) return FLCE_ERR_ALIGN;
+  return FLCE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
+        int64_t V, const flce_options* opt_in, float* loss, float* lse_out, uint16_t* dH, void* dW,
+        bool backward, void* workspace, size_t ws_bytes, int32_t* status, void* stream_v) {
+  flce_options o;
+  flce_default_options(&o);
+  if (opt_in != nullptr) o = *opt_in;
+  if (H == nullptr || W == nullptr || labels == nullptr || loss == nullptr || workspace == nullptr)
+    return FLCE_ERR_NULL;
+  int rc = check_shape(N, D, V);
+  if (rc != FLCE_OK) return rc;
+  rc = check_options(o);
+  if (rc != FLCE_OK) return rc;
+  if (!aligned16(H) || !aligned16(W) || !aligned16(labels) || !aligned16(workspace) ||
+      (lse_out && !aligned16(lse_out)) || (dH && !aligned16(dH)) || (dW && !aligned16(dW)) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return FLCE_ERR_ALIGN;
+  int sms = 0;
+  rc = device_info(&sms);
+  if (rc != FLCE_OK) return rc;
+  Plan P;
+  rc = make_plan(N, D, V, o, sms, &P);
+  if (rc != FLCE_OK) return rc;
+  if (ws_bytes < P.total) return FLCE_ERR_WORKSPACE;
+  if (!backward) {
+    dH = nullptr;
+    dW = nullptr;
+  }
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float2* part = reinterpret_cast<float2*>(ws + P.off_part);
+  float* zt = reinterpret_cast<float*>(ws + P.off_zt);
+  float* nll = reinterpret_cast<float*>(ws + P.off_nll);
+  float* lse = lse_out ? lse_out : reinterpret_cast<float*>(ws + P.off_lse);
+  float* scal = reinterpret_cast<float*>(ws + P.off_scal);  // [0] scale
+  int32_t* nvalid = reinterpret_cast<int32_t*>(ws + P.off_scal + 4);
+  uint16_t* G = reinterpret_cast<uint16_t*>(ws + P.off_g);
+  float* dh_acc = reinterpret_cast<float*>(ws + P.off_dhacc);
+  float* dw_acc = reinterpret_cast<float*>(ws + P.off_dwacc);
+  const int64_t tmo = o.timeout_ns > 0 ? o.timeout_ns : kDefaultTimeoutNs;
+
+  if (status != nullptr && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+
+  CUtensorMap mH_k, mW_k;
+  if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) || !encode_bf16(&mW_k, W, D, V, D, BK, BN))
+    return FLCE_ERR_CUDA;
+
+  // ---- 1. forward LSE GEMM ----
+  GemmParams g{};
+  g.a_mn_major = 0;
+  g.b_mn_major = 0;
+  g.m_blocks = P.m_blocks;
+  g.n_blocks = P.v_tiles;
+  g.k_blocks = static_cast<int>(ceil_div(D, BK));
+  g.splits = P.splits;
+  g.num_units = P.splits * P.m_blocks;
+  g.group_m = 1;
+  g.idesc = make_idesc_bf16_f32(BM, BN, 0, 0);
+  g.timeout_ns = tmo;
+  g.status = status;
+  g.m_valid = static_cast<int>(N);
+  g.n_valid = static_cast<int>(V);
+  g.labels = labels;
+  g.row_base = 0;
+  g.col_base = 0;
+  g.ignore_index = o.ignore_index;
+  g.part = part;
+  g.zt = zt;
+  if (launch_gemm_lse(mH_k, mW_k, g, std::min(g.num_units, sms), st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+
+  // ---- 2./3. merge and reduce ----
+  if (launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V), P.m_blocks,
+                       P.splits, o.ignore_index, lse, nll, st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (launch_loss_reduce(nll, labels, static_cast<int>(N), static_cast<int>(V), o.ignore_index,
+                         o.reduction, o.grad_scale, o.normalizer, loss, scal, nvalid, status,
+                         st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (dH == nullptr && dW == nullptr) return FLCE_OK;
+
+  // ---- 4. backward, token block outer, vocabulary chunk inner ----
+  const int64_t rows_b = ceil_div(P.n_block, BM) * BM;
+  CUtensorMap mH_mn, mW_mn, mG_mn, mG_k;
+  if (!encode_bf16(&mH_mn, H, D, N, D, 64, BK) || !encode_bf16(&mW_mn, W, D, V, D, 64, BK) ||
+      !encode_bf16(&mG_mn, G, P.v_chunk, rows_b, P.v_chunk, 64, BK) ||
+      !encode_bf16(&mG_k, G, P.v_chunk, rows_b, P.v_chunk, BK, BM))
+    return FLCE_ERR_CUDA;
+  const bool dw_bf16 = o.dw_dtype == FLCE_DTYPE_BF16;
+
+  for (int b = 0; b < P.n_nblocks; ++b) {
+    const int64_t b0 = static_cast<int64_t>(b) * P.n_block;
+    const int nb_len = static_cast<int>(std::min<int64_t>(P.n_block, N - b0));
+    for (int c = 0; c < P.n_chunks; ++c) {
+      const int64_t c0 = static_cast<int64_t>(c) * P.v_chunk;
+      const int c_len = static_cast<int>(std::min<int64_t>(P.v_chunk, V - c0));
+
+      // G chunk: recompute Z_bc and form (softmax - onehot) * scale in bf16.
+      GemmParams q{};
+      q.a_mn_major = 0;
+      q.b_mn_major = 0;
+      q.a_mn0 = static_cast<int>(b0);
+      q.b_mn0 = static_cast<int>(c0);
+      q.m_blocks = static_cast<int>(ceil_div(nb_len, BM));
+      q.n_blocks = static_cast<int>(ceil_div(c_len, BN));
+      q.k_blocks = static_cast<int>(ceil_div(D, BK));
+      q.num_units = q.m_blocks * q.n_blocks;
+      q.group_m = q.m_blocks;
+      q.idesc = make_idesc_bf16_f32(BM, BN, 0, 0);
+      q.timeout_ns = tmo;
+      q.status = status;
+      q.m_valid = nb_len;
+      q.n_valid = c_len;
+      q.labels = labels;
+      q.row_base = static_cast<int>(b0);
+      q.col_base = static_cast<int>(c0);
+      q.ignore_index = o.ignore_index;
+      q.lse = lse;
+      q.scale = scal;
+      q.g_out = G;
+      q.g_ld = P.v_chunk;
+      if (launch_gemm_grad(mH_k, mW_k, q, std::min(q.num_units, sms), st) != cudaSuccess)
+        return FLCE_ERR_CUDA;
+
+      if (dW != nullptr) {
+        // dW rows [c0, c0 + c_len) (+)= G_bc^T H_b: M = vocabulary, N = hidden, K = tokens.
+        GemmParams w{};
+        w.a_mn_major = 1;
+        w.b_mn_major = 1;
+        w.b_k0 = static_cast<int>(b0);
+        w.m_blocks = static_cast<int>(ceil_div(c_len, BM));
+        w.n_blocks = static_cast<int>(ceil_div(D, BN));
+        w.k_blocks = static_cast<int>(ceil_div(nb_len, BK));
+        w.num_units = w.m_blocks * w.n_blocks;
+        w.group_m = std::min(w.m_blocks, 16);
+        w.idesc = make_idesc_bf16_f32(BM, BN, 1, 1);
+        w.timeout_ns = tmo;
+        w.status = status;
+        w.m_valid = c_len;
+        w.n_valid = static_cast<int>(D);
+        const bool first = b == 0, last = b == P.n_nblocks - 1;
+        if (!dw_bf16) {
+          w.out_f32 = static_cast<float*>(dW);
+          w.out_f32_ld = D;
+          w.out_f32_row0 = static_cast<int>(c0);
+          w.out_mode = first ? OUT_STORE_F32 : OUT_ADD_F32;
+        } else if (P.n_nblocks == 1) {
+          w.out_bf16 = static_cast<uint16_t*>(dW);
+          w.out_bf16_ld = D;
+          w.out_bf16_row0 = static_cast<int>(c0);
+          w.out_mode = OUT_STORE_BF16;
+        } else {
+          w.out_f32 = dw_acc;
+          w.out_f32_ld = D;
+          w.out_f32_row0 = static_cast<int>(c0);
+          w.out_bf16 = static_cast<uint16_t*>(dW);
+          w.out_bf16_ld = D;
+          w.out_bf16_row0 = static_cast<int>(c0);
+          w.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
+        }
+        if (launch_gemm_f32(mG_mn, mH_mn, w, std::min(w.num_units, sms), st) != cudaSuccess)
+          return FLCE_ERR_CUDA;
+      }
+
+      if (dH != nullptr) {
+        // dH rows [b0, b0 + nb_len) (+)= G_bc W_c: M = tokens, N = hidden, K = vocabulary.
+        GemmParams h{};
+        h.a_mn_major = 0;
+        h.b_mn_major = 1;
+        h.b_k0 = static_cast<int>(c0);
+        h.m_blocks = static_cast<int>(ceil_div(nb_len, BM));
+        h.n_blocks = static_cast<int>(ceil_div(D, BN));
+        h.k_blocks = static_cast<int>(ceil_div(c_len, BK));
+        h.num_units = h.m_blocks * h.n_blocks;
+        h.group_m = std::min(h.m_blocks, 16);
+        h.idesc = make_idesc_bf16_f32(BM, BN, 0, 1);
+        h.timeout_ns = tmo;
+        h.status = status;
+        h.m_valid = nb_len;
+        h.n_valid = static_cast<int>(D);
+        const bool first = c == 0, last = c == P.n_chunks - 1;
+        h.out_f32 = dh_acc;
+        h.out_f32_ld = D;
+        h.out_f32_row0 = 0;
+        h.out_bf16 = dH;
+        h.out_bf16_ld = D;
+        h.out_bf16_row0 = static_cast<int>(b0);
+        if (P.n_chunks == 1)
+          h.out_mode = OUT_STORE_BF16;
+        else
+          h.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
+        if (launch_gemm_f32(mG_k, mW_mn, h, std::min(h.num_units, sms), st) != cudaSuccess)
+          return FLCE_ERR_CUDA;
+      }
+    }
+  }
+  return FLCE_OK;
+}
+
+}  // namespace
+}  // namespace flce
+
+extern "C" {
+
+void flce_default_options(flce_options* opt) {
+  if (opt == nullptr) return;
+  std::memset(opt, 0, sizeof(*opt));
+  opt->ignore_index = -100;
+  opt->reduction = FLCE_REDUCTION_MEAN;
+  opt->grad_scale = 1.0f;
+  opt->normalizer = 0.0f;
+  opt->dw_dtype = FLCE_DTYPE_F32;
+  opt->timeout_ns = 0;
+}
+
+int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt, size_t* bytes) {
+  if (bytes == nullptr) return FLCE_ERR_NULL;
+  flce_options o;
+  flce_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  int rc = flce::check_shape(N, D, V);
+  if (rc != FLCE_OK) return rc;
+  rc = flce::check_options(o);
+  if (rc != FLCE_OK) return rc;
+  // The vocabulary-range split count depends on the SM count; plan for the
+  // largest split count that choose_splits can return so that the size does not
+  // depend on the device (and can be asked for without one).
+  flce_options big = o;
+  if (big.v_splits == 0) big.v_splits = static_cast<int32_t>(std::min<int64_t>(
+                                            flce::ceil_div(V, flce::BN), 128));
+  flce::Plan P;
+  rc = flce::make_plan(N, D, V, big, 1, &P);
+  if (rc != FLCE_OK) return rc;
+  *bytes = P.total;
+  return FLCE_OK;
+}
+
+int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N,
+                          int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
+                          uint16_t* dH, void* dW, void* workspace, size_t ws_bytes,
+                          int32_t* status, void* stream) {
+  return flce::run(H, W, labels, N, D, V, opt, loss, lse, dH, dW, true, workspace, ws_bytes,
+                   status, stream);
+}
+
+int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
+                 int64_t V, const flce_options* opt, float* loss, float* lse, void* workspace,
+                 size_t ws_bytes, int32_t* status, void* stream) {
+  return flce::run(H, W, labels, N, D, V, opt, loss, lse, nullptr, nullptr, false, workspace,
+                   ws_bytes, status, stream);
+}
+
+int flce_check_status(const int32_t* status, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (status == nullptr) return FLCE_OK;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return h;
+}
+
+const char* flce_status_string(int code) {
+  switch (code) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_NULL: return "a required pointer is NULL";
+    case FLCE_ERR_SHAPE: return "N, D or V out of range";
+    case FLCE_ERR_ALIGN: return "pointer not 16-byte aligned or D not a multiple of 8";
+    case FLCE_ERR_WORKSPACE: return "workspace too small";
+    case FLCE_ERR_OPTION: return "option out of range";
+    case FLCE_ERR_CUDA: return "CUDA call failed";
+    case FLCE_ERR_DEVICE: return "device is not an sm_103 GPU";
+    case FLCE_ERR_LABEL_RANGE: return "a label is outside [0, V) and is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

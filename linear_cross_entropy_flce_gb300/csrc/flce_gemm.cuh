@@ -1,0 +1,416 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with three fused
+// epilogues. Every product of fused linear cross-entropy runs through it:
+//
+//   LSE  : Z = H W^T tile by tile, accumulated in TMEM; the epilogue keeps a
+//          per-token running max and sum of exponentials across the vocabulary
+//          tiles of a work unit and extracts the target logit ("Liger Kernel:
+//          Fused Triton Kernels for LLM Training", The Architecture, 1. steps
+//          2-5: in-SRAM tile product, online LogSumExp, immediate target
+//          extraction, no logits written).
+//   GRAD : Z recomputed tile by tile; the epilogue forms
+//          G = (exp(z - lse) - [v = y]) * scale in bf16 and writes one chunk of G
+//          (same page, 2. In-Kernel Gradient Computation: recompute the tile
+//          logits from the saved LSE, derive dL/dz in the kernel).
+//   F32  : plain product with an fp32 store, fp32 accumulate, or accumulate then
+//          round to bf16 — used for dW = G^T H and dH = G W (same page, 2.).
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0     : TMA producer (one thread) — streams A/B K-slices into a ring of
+//                shared-memory stages.
+//   warp 1     : TMEM allocator and MMA issuer (one thread) — tcgen05.mma
+//                128 x 256 x 16 steps into one of two TMEM accumulators.
+//   warps 2..5 : epilogue — warp w reads TMEM lanes 32*(w%4) .. +31, so each
+//                thread owns one output row of the 128-row tile.
+// Every wait is bounded (see mbar_wait_bounded); on a timeout the CTA records
+// FLCE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+
+#include "flce_gemm_params.h"
+#include "ptx.cuh"
+
+namespace flce {
+
+template <int kEpi>
+__device__ __forceinline__ void unit_tiles(const GemmParams& p, int u, int& m_blk, int& n_begin,
+                                           int& n_end) {
+  if constexpr (kEpi == EPI_LSE) {
+    const int s = u / p.m_blocks;
+    m_blk = u - s * p.m_blocks;
+    n_begin = static_cast<int>((static_cast<int64_t>(s) * p.n_blocks) / p.splits);
+    n_end = static_cast<int>((static_cast<int64_t>(s + 1) * p.n_blocks) / p.splits);
+  } else {
+    const int per_group = p.group_m * p.n_blocks;
+    const int g = u / per_group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.m_blocks - first_m, p.group_m);
+    const int r = u - g * per_group;
+    n_begin = r / gm;
+    m_blk = first_m + (r - n_begin * gm);
+    n_end = n_begin + 1;
+  }
+}
+
+__device__ __forceinline__ void record_status(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+// ---- epilogue bodies ---------------------------------------------------------------
+
+struct LseState {
+  float m;   // running max of z
+  float s;   // running sum of exp(z - m)
+  float zt;  // target logit
+  bool found;
+};
+
+// One 32-column chunk of the logits tile for this thread's row.
+__device__ __forceinline__ void lse_chunk(const float (&v)[32], int col_local, int n_valid,
+                                          int rel_target, LseState& st) {
+  float x[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) x[k] = v[k];
+  if (col_local + 32 > n_valid) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (col_local + k >= n_valid) x[k] = -INFINITY;
+  }
+  if (static_cast<unsigned>(rel_target) < 32u) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k == rel_target) st.zt = v[k];
+    st.found = true;
+  }
+  float c0 = fmaxf(x[0], x[1]), c1 = fmaxf(x[2], x[3]);
+#pragma unroll
+  for (int k = 4; k < 32; k += 4) {
+    c0 = fmaxf(c0, fmaxf(x[k], x[k + 1]));
+    c1 = fmaxf(c1, fmaxf(x[k + 2], x[k + 3]));
+  }
+  const float mn = fmaxf(st.m, fmaxf(c0, c1));
+  if (mn == -INFINITY) return;
+  const float ms = mn * kLog2e;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    s0 += ex2_approx(fmaf(x[k + 0], kLog2e, -ms));
+    s1 += ex2_approx(fmaf(x[k + 1], kLog2e, -ms));
+    s2 += ex2_approx(fmaf(x[k + 2], kLog2e, -ms));
+    s3 += ex2_approx(fmaf(x[k + 3], kLog2e, -ms));
+  }
+  st.s = st.s * ex2_approx((st.m - mn) * kLog2e) + ((s0 + s1) + (s2 + s3));
+  st.m = mn;
+}
+
+// G for one 32-column chunk: bf16 (exp(z - lse) - [v = y]) * sc; 0 past n_valid.
+__device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, int n_valid,
+                                           int rel_target, float nlse2, float sc,
+                                           uint16_t* gdst) {
+  float g[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) g[k] = ex2_approx(fmaf(v[k], kLog2e, nlse2)) * sc;
+  if (static_cast<unsigned>(rel_target) < 32u) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k == rel_target) g[k] -= sc;
+  }
+  if (col_local + 32 > n_valid) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (col_local + k >= n_valid) g[k] = 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    st_global_v4(gdst + q * 8, pack_bf16x2(g[q * 8 + 0], g[q * 8 + 1]),
+                 pack_bf16x2(g[q * 8 + 2], g[q * 8 + 3]), pack_bf16x2(g[q * 8 + 4], g[q * 8 + 5]),
+                 pack_bf16x2(g[q * 8 + 6], g[q * 8 + 7]));
+  }
+}
+
+__device__ __forceinline__ void f32_chunk(const float (&v)[32], const GemmParams& p, int row,
+                                          int col) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c = col + 4 * j;
+    if (c >= p.n_valid) break;
+    float a = v[4 * j + 0], b = v[4 * j + 1], cc = v[4 * j + 2], d = v[4 * j + 3];
+    if (p.out_mode == OUT_STORE_F32 || p.out_mode == OUT_ADD_F32) {
+      float* dst = p.out_f32 + static_cast<int64_t>(p.out_f32_row0 + row) * p.out_f32_ld + c;
+      if (p.out_mode == OUT_ADD_F32) {
+        const float4 o = ld_global_v4f(dst);
+        a += o.x; b += o.y; cc += o.z; d += o.w;
+      }
+      st_global_v4(dst, __float_as_uint(a), __float_as_uint(b), __float_as_uint(cc),
+                   __float_as_uint(d));
+    } else {
+      if (p.out_mode == OUT_ADD_TO_BF16) {
+        const float* src =
+            p.out_f32 + static_cast<int64_t>(p.out_f32_row0 + row) * p.out_f32_ld + c;
+        const float4 o = ld_global_v4f(src);
+        a += o.x; b += o.y; cc += o.z; d += o.w;
+      }
+      uint16_t* dst = p.out_bf16 + static_cast<int64_t>(p.out_bf16_row0 + row) * p.out_bf16_ld + c;
+      const uint32_t lo = pack_bf16x2(a, b), hi = pack_bf16x2(cc, d);
+      asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(dst), "r"(lo), "r"(hi) : "memory");
+    }
+  }
+}
+
+// ---- the kernel --------------------------------------------------------------------
+
+template <int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // bars: full[kStages] | empty[kStages] | tfull[2] | tempty[2] | drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t stage0 = smem_u32(smem);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
+  auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * kStages + 2 + a); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int m_blk, n_begin, n_end;
+        unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t sa = stage0 + stage * kStageBytes;
+            const uint32_t sb = sa + kABytes;
+            const int kx = kb * BK;
+            if (!p.a_mn_major) {
+              tma_load_2d(sa, &tmA, kx + p.a_k0, m_blk * BM + p.a_mn0, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d(sa + j * kMnBoxBytes, &tmA, m_blk * BM + 64 * j + p.a_mn0, kx + p.a_k0,
+                            fb);
+            }
+            if (!p.b_mn_major) {
+              tma_load_2d(sb, &tmB, kx + p.b_k0, n_blk * BN + p.b_mn0, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * kMnBoxBytes, &tmB, n_blk * BN + 64 * j + p.b_mn0, kx + p.b_k0,
+                            fb);
+            }
+            issued_mask |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        record_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // Drain: every load this thread issued must land before the CTA exits.
+      const volatile int no_abort = 0;
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s))
+          mbar_wait_bounded(full_bar(s), (issued_par >> s) & 1u, 1000000000ull, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued_any = false;
+      const bool a_mn = p.a_mn_major != 0, b_mn = p.b_mn_major != 0;
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        int m_blk, n_begin, n_end;
+        unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
+          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, tmo, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = stage0 + stage * kStageBytes;
+            const uint32_t sb = sa + kABytes;
+#pragma unroll
+            for (int k = 0; k < BK / UK; ++k) {
+              const uint64_t da = a_mn ? make_sw128_desc(sa + k * (UK * 128), kMnBoxBytes, 1024)
+                                       : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
+              const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
+                                       : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
+              umma_bf16(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            issued_any = true;
+            umma_commit(empty_bar(stage));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(tfull_bar(acc));
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_status(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      if (issued_any) {
+        // Drain: all MMAs of this thread complete before TMEM is freed.
+        const volatile int no_abort = 0;
+        umma_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, 1000000000ull, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    float scale_v = 0.f;
+    if constexpr (kEpi == EPI_GRAD) scale_v = *p.scale;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      int m_blk, n_begin, n_end;
+      unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+      const int prow = m_blk * BM + row;  // row of the product
+      const bool row_ok = prow < p.m_valid;
+      int y = -1;
+      if constexpr (kEpi != EPI_F32) {
+        if (row_ok) {
+          const int lab = p.labels[p.row_base + prow];
+          y = (lab == p.ignore_index) ? -1 : lab;
+        }
+      }
+      LseState st{-INFINITY, 0.f, 0.f, false};
+      float nlse2 = 0.f, sc = 0.f;
+      if constexpr (kEpi == EPI_GRAD) {
+        if (row_ok) {
+          nlse2 = -p.lse[p.row_base + prow] * kLog2e;
+          sc = (y >= 0) ? scale_v : 0.f;
+        }
+      }
+      for (int n_blk = n_begin; n_blk < n_end; ++n_blk) {
+        int got = 0;
+        if (lane == 0) got = mbar_wait_bounded(tfull_bar(acc), acc_phase, tmo, abort_flag) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+          const int col = n_blk * BN + c * 32;  // product column
+          if constexpr (kEpi == EPI_LSE) {
+            lse_chunk(v, col, p.n_valid, y - (p.col_base + col), st);
+          } else if constexpr (kEpi == EPI_GRAD) {
+            grad_chunk(v, col, p.n_valid, y - (p.col_base + col), nlse2, sc,
+                       p.g_out + static_cast<int64_t>(prow) * p.g_ld + col);
+          } else {
+            if (row_ok && col < p.n_valid) f32_chunk(v, p, prow, col);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if constexpr (kEpi == EPI_LSE) {
+        if (ok) {
+          p.part[static_cast<int64_t>(u) * BM + row] = make_float2(st.m, st.s);
+          if (row_ok && st.found) p.zt[p.row_base + prow] = st.zt;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) record_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace flce

@@ -1,0 +1,78 @@
+// Tile constants and launch parameters of the tcgen05 GEMM (flce_gemm.cuh),
+// shared with the host code that plans and launches it.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <vector_types.h>
+
+namespace flce {
+
+constexpr int BM = 128;  // tile rows (tokens, or vocabulary ids for dW)
+constexpr int BN = 256;  // tile columns
+constexpr int BK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int UK = 16;   // K per tcgen05.mma for 16-bit inputs
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
+constexpr uint32_t kMnBoxBytes = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum EpiKind { EPI_LSE = 0, EPI_GRAD = 1, EPI_F32 = 2 };
+enum OutMode { OUT_STORE_F32 = 0, OUT_ADD_F32 = 1, OUT_ADD_TO_BF16 = 2, OUT_STORE_BF16 = 3 };
+
+constexpr int kStatusTimeout = 9;  // FLCE_ERR_TIMEOUT
+
+// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
+//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
+//   bit 15 A major (1 = MN-major), bit 16 B major, bits 17-22 N >> 3, bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int M, int N, int a_mn_major,
+                                                           int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major & 1) << 15) |
+         (static_cast<uint32_t>(b_mn_major & 1) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+struct GemmParams {
+  // operand geometry: coordinates of tile (m, n, k) in the tensor maps are
+  //   K-major  operand: x = k*BK + k0,         y = mn*BLOCK + mn0
+  //   MN-major operand: x = mn*BLOCK + 64j + mn0, y = k*BK + k0
+  int a_mn_major, b_mn_major;
+  int a_mn0, a_k0, b_mn0, b_k0;
+  int m_blocks, n_blocks, k_blocks;
+  int num_units;
+  int splits;   // EPI_LSE: vocabulary ranges; unit u = s * m_blocks + m
+  int group_m;  // other epilogues: tile raster, groups of group_m row blocks
+  uint32_t idesc;
+  int64_t timeout_ns;
+  int32_t* status;
+  int m_valid;  // rows of the product that exist
+  int n_valid;  // columns of the product that exist
+  // EPI_LSE / EPI_GRAD
+  const int32_t* labels;  // labels[row_base + row]
+  int row_base;
+  int col_base;           // vocabulary id of product column 0
+  int ignore_index;
+  float2* part;           // EPI_LSE: [num_units][BM] (max, sum exp)
+  float* zt;              // EPI_LSE: target logit per token
+  const float* lse;       // EPI_GRAD: lse[row_base + row]
+  const float* scale;     // EPI_GRAD: device scalar grad_scale / n
+  uint16_t* g_out;        // EPI_GRAD: G chunk, row stride g_ld elements
+  int64_t g_ld;
+  // EPI_F32
+  float* out_f32;
+  int64_t out_f32_ld;
+  int out_f32_row0;
+  uint16_t* out_bf16;
+  int64_t out_bf16_ld;
+  int out_bf16_row0;
+  int out_mode;
+};
+
+}  // namespace flce

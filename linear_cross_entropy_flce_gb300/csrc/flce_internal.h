@@ -1,0 +1,34 @@
+// Internal launch interface shared by the host API and the kernel translation
+// units of the library. Not part of the public C ABI (include/flce.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "flce_gemm_params.h"
+
+namespace flce {
+
+cudaError_t launch_gemm_lse(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                            int grid, cudaStream_t stream);
+cudaError_t launch_gemm_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_gemm_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                            int grid, cudaStream_t stream);
+
+// Per-token merge of the vocabulary-range partials into lse and the per-token
+// negative log-likelihood.
+cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
+                             int V, int m_blocks, int splits, int ignore_index, float* lse,
+                             float* nll, cudaStream_t stream);
+
+// One-block deterministic reduction: label validation, n_valid, the loss and
+// the gradient scale grad_scale / n (or / normalizer, or 1 for "sum").
+cudaError_t launch_loss_reduce(const float* nll, const int32_t* labels, int N, int V,
+                               int ignore_index, int reduction, float grad_scale,
+                               float normalizer, float* loss, float* scale, int32_t* n_valid,
+                               int32_t* status, cudaStream_t stream);
+
+}  // namespace flce

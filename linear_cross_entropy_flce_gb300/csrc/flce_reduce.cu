@@ -1,0 +1,123 @@
+// Per-token merge of the forward pass's vocabulary-range partials, and the
+// one-block deterministic loss reduction.
+//
+// The merge is the combination rule of the online log-sum-exp ("Liger Kernel:
+// Fused Triton Kernels for LLM Training", The Architecture, 1. step 3): for
+// partials (m_u, s_u) with s_u = sum exp(z - m_u) over disjoint vocabulary
+// ranges, M = max_u m_u and lse = M + log(sum_u s_u exp(m_u - M)). The loss is
+// the mean over non-ignored tokens of lse_i - z_{i,y_i} (same section, steps
+// 4-5; the mean of the page's simulation and of PyTorch's reduction="mean").
+#include <cmath>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+namespace {
+
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
+                                 const int32_t* __restrict__ labels, int N, int V, int m_blocks,
+                                 int splits, int ignore_index, float* __restrict__ lse,
+                                 float* __restrict__ nll) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int r = i / BM, l = i - (i / BM) * BM;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[(static_cast<int64_t>(s) * m_blocks + r) * BM + l].x);
+  float S = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float2 pr = part[(static_cast<int64_t>(s) * m_blocks + r) * BM + l];
+    S += pr.y * ex2f_approx((pr.x - M) * kLog2e);
+  }
+  const float L = M + logf(S);
+  lse[i] = L;
+  const int y = labels[i];
+  nll[i] = (y != ignore_index && y >= 0 && y < V) ? L - zt[i] : 0.f;
+}
+
+constexpr int kReduceThreads = 1024;
+
+__global__ void __launch_bounds__(kReduceThreads)
+    loss_reduce_kernel(const float* __restrict__ nll, const int32_t* __restrict__ labels, int N,
+                       int V, int ignore_index, int reduction, float grad_scale, float normalizer,
+                       float* loss, float* scale, int32_t* n_valid_out, int32_t* status) {
+  __shared__ double s_sum[kReduceThreads];
+  __shared__ int s_cnt[kReduceThreads];
+  __shared__ int s_bad[kReduceThreads];
+  const int t = threadIdx.x;
+  double acc = 0.0;
+  int cnt = 0, bad = 0;
+  for (int i = t; i < N; i += kReduceThreads) {
+    const int y = labels[i];
+    if (y == ignore_index) continue;
+    if (y < 0 || y >= V) {
+      bad = 1;
+      continue;
+    }
+    ++cnt;
+    acc += static_cast<double>(nll[i]);
+  }
+  s_sum[t] = acc;
+  s_cnt[t] = cnt;
+  s_bad[t] = bad;
+  __syncthreads();
+  for (int w = kReduceThreads / 2; w > 0; w >>= 1) {
+    if (t < w) {
+      s_sum[t] += s_sum[t + w];
+      s_cnt[t] += s_cnt[t + w];
+      s_bad[t] |= s_bad[t + w];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    const double total = s_sum[0];
+    const int n = s_cnt[0];
+    double l, sc;
+    if (reduction == 1) {  // sum
+      l = total;
+      sc = grad_scale;
+    } else if (normalizer > 0.f) {
+      l = total / normalizer;
+      sc = grad_scale / static_cast<double>(normalizer);
+    } else if (n > 0) {
+      l = total / n;
+      sc = grad_scale / static_cast<double>(n);
+    } else {
+      l = 0.0;
+      sc = 0.0;
+    }
+    *loss = static_cast<float>(l);
+    *scale = static_cast<float>(sc);
+    *n_valid_out = n;
+    if (s_bad[0] && status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, 8);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
+                             int V, int m_blocks, int splits, int ignore_index, float* lse,
+                             float* nll, cudaStream_t stream) {
+  const int threads = 256;
+  lse_merge_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(
+      part, zt, labels, N, V, m_blocks, splits, ignore_index, lse, nll);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_reduce(const float* nll, const int32_t* labels, int N, int V,
+                               int ignore_index, int reduction, float grad_scale,
+                               float normalizer, float* loss, float* scale, int32_t* n_valid,
+                               int32_t* status, cudaStream_t stream) {
+  loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(nll, labels, N, V, ignore_index, reduction,
+                                                       grad_scale, normalizer, loss, scale,
+                                                       n_valid, status);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

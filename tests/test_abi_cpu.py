@@ -1,0 +1,107 @@
+"""The C-ABI library loads without a GPU, exports every function that
+include/flce.h declares, and rejects bad arguments on the host before any
+device work (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_cross_entropy_flce_gb300 as flce
+from linear_cross_entropy_flce_gb300 import _binding
+
+HEADER = _binding.HEADER_PATH
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_forward_backward",
+                            "flce_forward", "flce_check_status", "flce_status_string"])
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(flce.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_default_options():
+    o = flce.make_options()
+    assert (o.ignore_index, o.reduction, o.grad_scale, o.normalizer, o.dw_dtype) == (-100, 0, 1.0, 0.0, 0)
+    assert (o.v_splits, o.n_block, o.v_chunk, o.timeout_ns) == (0, 0, 0, 0)
+    assert ctypes.sizeof(flce.Options) == 48
+
+
+def test_workspace_is_far_below_logits():
+    # The bound is one G chunk plus small per-token arrays; at tile-sized
+    # problems the 128 x 256 tile rounding dominates instead.
+    assert flce.workspace_size(64, 128, 1000) < 1 << 20
+    for N, D, V in [(4096, 2048, 32000), (8192, 4096, 128256),
+                    (16384, 3584, 152064), (32768, 4096, 128256)]:
+        ws = flce.workspace_size(N, D, V)
+        assert 0 < ws < N * V * 4 / 4, (N, D, V, ws)
+
+
+def test_workspace_grows_with_requested_chunk():
+    a = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=4096))
+    b = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=16384))
+    assert b - a == pytest.approx(8192 * (16384 - 4096) * 2, rel=0.01)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=0, D=128, V=10), flce.FLCE_ERR_SHAPE),
+    (dict(N=8, D=0, V=10), flce.FLCE_ERR_SHAPE),
+    (dict(N=8, D=128, V=0), flce.FLCE_ERR_SHAPE),
+    (dict(N=8, D=100, V=10), flce.FLCE_ERR_ALIGN),
+])
+def test_workspace_size_rejects_bad_shapes(kw, code):
+    out = ctypes.c_size_t()
+    assert flce.lib.flce_workspace_size(kw["N"], kw["D"], kw["V"], None, ctypes.byref(out)) == code
+
+
+@pytest.mark.parametrize("opt,code", [
+    (dict(reduction=7), flce.FLCE_ERR_OPTION),
+    (dict(dw_dtype=3), flce.FLCE_ERR_OPTION),
+    (dict(v_chunk=300), flce.FLCE_ERR_OPTION),
+    (dict(n_block=100), flce.FLCE_ERR_OPTION),
+    (dict(timeout_ns=-1), flce.FLCE_ERR_OPTION),
+])
+def test_workspace_size_rejects_bad_options(opt, code):
+    o = flce.make_options()
+    for k, v in opt.items():
+        setattr(o, k, v)
+    out = ctypes.c_size_t()
+    assert flce.lib.flce_workspace_size(64, 128, 1000, ctypes.byref(o), ctypes.byref(out)) == code
+
+
+def _call(H=0x1000, W=0x2000, y=0x3000, N=64, D=128, V=1000, loss=0x4000, ws=0x5000,
+          ws_bytes=1 << 30, status=None, opts=None):
+    return flce.lib.flce_forward_backward(H, W, y, N, D, V, ctypes.byref(opts) if opts else None,
+                                          loss, None, None, None, ws, ws_bytes, status, None)
+
+
+def test_host_rejections_happen_before_device_work():
+    assert _call(H=None) == flce.FLCE_ERR_NULL
+    assert _call(W=None) == flce.FLCE_ERR_NULL
+    assert _call(y=None) == flce.FLCE_ERR_NULL
+    assert _call(loss=None) == flce.FLCE_ERR_NULL
+    assert _call(ws=None) == flce.FLCE_ERR_NULL
+    assert _call(N=-1) == flce.FLCE_ERR_SHAPE
+    assert _call(D=12) == flce.FLCE_ERR_ALIGN
+    assert _call(H=0x1008) == flce.FLCE_ERR_ALIGN
+    assert _call(ws=0x5004) == flce.FLCE_ERR_ALIGN
+    o = flce.make_options()
+    o.reduction = 5
+    assert _call(opts=o) == flce.FLCE_ERR_OPTION
+
+
+def test_status_strings():
+    for code in range(0, 10):
+        assert flce.status_string(code) and flce.status_string(code) != "unknown status"
+    assert flce.status_string(1234) == "unknown status"

@@ -1,0 +1,194 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU float64
+oracle on the same seeded inputs, plus edge cases and invariants that hold at
+any size."""
+import numpy as np
+import pytest
+
+import flce_inputs
+import oracle
+from flce_testlib import assert_within, bf16_tensor_to_f64, compare, tensor_to_f64, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import linear_cross_entropy_flce_gb300 as flce
+
+
+def _inputs(N, D, V, seed=0, w_std=0.05, h_scale=1.0, p_ignore=0.0, labels="uniform"):
+    wl = flce_inputs.Workload("custom", N, D, V, h_scale, w_std, labels, p_ignore, seed=seed)
+    return flce_inputs.make_inputs(wl)
+
+
+def _run_and_compare(Hb, Wb, y, **opts):
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab, **opts)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    ref_kw = {k: opts[k] for k in ("reduction", "grad_scale", "normalizer", "ignore_index") if k in opts}
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y, **ref_kw)
+    errs = compare(res, ref)
+    print(errs)
+    assert_within(errs)
+    return res, ref
+
+
+def test_tiny_workload_full_parity():
+    Hb, Wb, y = flce_inputs.make_inputs(flce_inputs.get("tiny"))
+    _run_and_compare(Hb, Wb, y)
+
+
+@pytest.mark.parametrize("opts", [
+    {},
+    {"v_chunk": 512, "n_block": 128},
+    {"v_chunk": 256, "n_block": 256, "v_splits": 3},
+    {"v_chunk": 768, "n_block": 128, "dw_dtype": "bfloat16"},
+    {"dw_dtype": "bfloat16"},
+])
+def test_ragged_shapes_and_plans(opts):
+    # N, V not multiples of the 128 x 256 tile; D not a multiple of 64.
+    Hb, Wb, y = _inputs(300, 200, 1500, seed=3, p_ignore=0.07)
+    _run_and_compare(Hb, Wb, y, **opts)
+
+
+@pytest.mark.parametrize("N,D,V", [(1, 8, 1), (1, 64, 2), (129, 136, 257), (127, 8, 300), (512, 1024, 4096)])
+def test_small_and_degenerate_shapes(N, D, V):
+    Hb, Wb, y = _inputs(N, D, V, seed=N + V)
+    _run_and_compare(Hb, Wb, y)
+
+
+def test_labels_at_vocabulary_edges():
+    Hb, Wb, y = _inputs(256, 128, 1000, seed=5)
+    y[:64] = 0
+    y[64:128] = 999
+    _run_and_compare(Hb, Wb, y)
+
+
+@pytest.mark.parametrize("opts", [
+    {"reduction": "sum"},
+    {"grad_scale": 0.25},
+    {"normalizer": 1000.0},
+    {"ignore_index": 7},
+])
+def test_reduction_and_scaling_options(opts):
+    Hb, Wb, y = _inputs(200, 256, 700, seed=9, p_ignore=0.1)
+    if opts.get("ignore_index") == 7:
+        y[y == -100] = 7
+    _run_and_compare(Hb, Wb, y, **opts)
+
+
+def test_all_tokens_ignored():
+    Hb, Wb, y = _inputs(130, 64, 400, seed=11)
+    y[:] = -100
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab, v_chunk=256)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    assert float(res.loss.item()) == 0.0
+    assert torch.count_nonzero(res.dH).item() == 0
+    assert torch.count_nonzero(res.dW).item() == 0
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y)
+    assert np.max(np.abs(res.lse.double().cpu().numpy() - ref["lse"])) <= 2e-3
+
+
+def test_zero_weights_closed_form():
+    """W = 0: loss and every lse equal log V, dH = 0, dW_v = sum_valid (1/V - [y=v]) h_i / n."""
+    N, D, V = 300, 128, 1000
+    Hb, _, y = _inputs(N, D, V, seed=12, p_ignore=0.1)
+    Wb = np.zeros((V, D), dtype=np.uint16)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab, v_chunk=256)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    assert float(res.loss.item()) == pytest.approx(np.log(V), rel=1e-6)
+    assert np.max(np.abs(res.lse.cpu().numpy() - np.log(V))) < 1e-5
+    assert torch.count_nonzero(res.dH).item() == 0
+    Hd = flce_inputs.bf16_bits_to_f64(Hb)
+    valid = y != -100
+    n = valid.sum()
+    expect = np.tile(Hd[valid].sum(0) / V / n, (V, 1))
+    for i in np.nonzero(valid)[0]:
+        expect[y[i]] -= Hd[i] / n
+    got = res.dW.double().cpu().numpy()
+    assert np.linalg.norm(got - expect) / np.linalg.norm(expect) < 5e-3
+
+
+def test_ignored_rows_have_exactly_zero_dh():
+    Hb, Wb, y = _inputs(400, 256, 2000, seed=13, p_ignore=0.2)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    ign = torch.from_numpy(y == -100).to(res.dH.device)
+    assert torch.count_nonzero(res.dH[ign]).item() == 0
+
+
+def test_dw_columns_sum_to_zero():
+    """sum_v dW_v = sum_i (sum_v g_iv) h_i = 0 (rows of softmax - onehot sum to 0)."""
+    Hb, Wb, y = _inputs(512, 256, 3000, seed=14)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    colsum = res.dW.double().sum(0)
+    scale = res.dW.double().abs().sum(0)
+    assert float((colsum.abs() / scale).max()) < 5e-3
+
+
+def test_run_to_run_bitwise_determinism():
+    Hb, Wb, y = _inputs(700, 512, 5000, seed=15, p_ignore=0.05)
+    H, W, lab = to_device(Hb, Wb, y)
+    a = flce.forward_backward(H, W, lab, v_chunk=1024, n_block=256)
+    b = flce.forward_backward(H, W, lab, v_chunk=1024, n_block=256)
+    torch.cuda.synchronize()
+    assert torch.equal(a.loss, b.loss) and torch.equal(a.lse, b.lse)
+    assert torch.equal(a.dH.view(torch.int16), b.dH.view(torch.int16))
+    assert torch.equal(a.dW, b.dW)
+
+
+def test_optional_outputs_and_forward_only():
+    Hb, Wb, y = _inputs(300, 128, 900, seed=16, p_ignore=0.1)
+    H, W, lab = to_device(Hb, Wb, y)
+    full = flce.forward_backward(H, W, lab)
+    only_dh = flce.forward_backward(H, W, lab, need_dw=False)
+    only_dw = flce.forward_backward(H, W, lab, need_dh=False)
+    fwd = flce.forward(H, W, lab)
+    torch.cuda.synchronize()
+    assert torch.equal(full.dH.view(torch.int16), only_dh.dH.view(torch.int16))
+    assert torch.equal(full.dW, only_dw.dW)
+    assert torch.equal(full.loss, fwd.loss) and torch.equal(full.lse, fwd.lse)
+
+
+def test_label_out_of_range_sets_device_status():
+    Hb, Wb, y = _inputs(200, 64, 500, seed=17)
+    y[33] = 500
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    assert flce.check_status(res.status) == flce.FLCE_ERR_LABEL_RANGE
+    y[33] = -3
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    assert flce.check_status(res.status) == flce.FLCE_ERR_LABEL_RANGE
+
+
+def test_workspace_too_small_is_rejected():
+    Hb, Wb, y = _inputs(200, 64, 500, seed=18)
+    H, W, lab = to_device(Hb, Wb, y)
+    need = flce.workspace_size(200, 64, 500)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda:0")
+    with pytest.raises(flce.FLCEError) as e:
+        flce.forward_backward(H, W, lab, workspace=ws)
+    assert e.value.code == flce.FLCE_ERR_WORKSPACE
+
+
+def test_token_permutation_equivariance():
+    """Each token's logits row, lse and dH row depend only on that token, so
+    permuting whole 128-token blocks of rows permutes lse and dH bit for bit."""
+    Hb, Wb, y = _inputs(512, 256, 2000, seed=19, p_ignore=0.05)
+    perm = np.concatenate([np.arange(256, 384), np.arange(0, 128), np.arange(384, 512),
+                           np.arange(128, 256)])
+    a = flce.forward_backward(*to_device(Hb, Wb, y), v_splits=2)
+    b = flce.forward_backward(*to_device(Hb[perm], Wb, y[perm]), v_splits=2)
+    torch.cuda.synchronize()
+    pt = torch.from_numpy(perm).to(a.lse.device)
+    assert torch.equal(a.lse[pt], b.lse)
+    assert torch.equal(a.dH[pt].view(torch.int16), b.dH.view(torch.int16))
+    assert abs(float(a.loss.item()) - float(b.loss.item())) <= 1e-6 * abs(float(a.loss.item()))
+
+
+def test_llama2_like_workload_full_parity():
+    Hb, Wb, y = flce_inputs.make_inputs(flce_inputs.get("llama2"))
+    _run_and_compare(Hb, Wb, y)
