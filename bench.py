@@ -1,0 +1,388 @@
+"""Benchmark of fused linear cross-entropy forward+backward on GB300.
+
+One step = one call of flce_forward_backward (loss, lse, dH, dW) over one batch
+of the Llama-3-8B-shaped head workload: N = 8192 tokens (B=2, S=4096),
+D = 4096, V = 128256, H ~ N(0,1), W ~ N(0, 0.02^2) in bf16, Zipf(1.1) labels,
+10% ignored tokens. Inputs are seeded synthetic data.
+
+Reported (one JSON line on rank 0):
+  value      tokens/s over all ranks, inputs resident in device memory
+  tflops     8*N*V*D flops per step / step time (forward, recompute, two gradient GEMMs)
+  e2e        tokens/s through the public API with host buffers: H, W and labels
+             copied from pinned host memory and the loss read back, every step
+  roofline   the tcgen05 GEMM kernel (every heavy launch of the step) against the
+             measured bf16 matmul peak
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample of the workload
+  peak_extra_hbm_bytes  the library's workspace (its whole extra device memory)
+                        next to the N*V*4 bytes of fp32 logits an unfused head holds
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+For N > 1 the driver launches one process per GPU with torch.distributed.run;
+every rank runs the same workload (replicas, weak scaling) and the slowest
+rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import flce_inputs  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s & TFLOP/s vs GB300 BF16 peak; peak extra HBM bytes"
+UNIT = "tokens/s"
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Replicas:
+    """Host-side coordination of independent replicas: a barrier and the max of
+    a per-rank time. No data of the computation crosses ranks."""
+
+    def __init__(self, world: int, rank: int):
+        self.world, self.rank = world, rank
+        self.pg = None
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+_SAMPLE_CACHE = {}
+
+
+def cpu_oracle_sample(wl, tokens: int) -> dict:
+    """The float64 oracle, as it stands, on the first `tokens` tokens of the
+    workload (full V and D): loss, lse, dH for those tokens and dW from them.
+    Only the oracle call is timed; the seeded draw is made once per sample size."""
+    import oracle
+    key = (wl.name, tokens)
+    if key not in _SAMPLE_CACHE:
+        Hb, Wb, y = flce_inputs.make_inputs(wl, N=tokens)
+        _SAMPLE_CACHE.clear()
+        _SAMPLE_CACHE[key] = (flce_inputs.bf16_bits_to_f32(Hb), flce_inputs.bf16_bits_to_f32(Wb), y)
+    H, W, y = _SAMPLE_CACHE[key]
+    t0 = time.perf_counter()
+    oracle.flce(H, W, y)
+    dt = time.perf_counter() - t0
+    return {"seconds": dt, "tokens": tokens}
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, wl, world, rank):
+    """The reference arm: the float64 CPU oracle, each step a bounded sample."""
+    if rank != 0:
+        return 0
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, tokens)
+    times = [cpu_oracle_sample(wl, tokens)["seconds"] for _ in range(args.steps)]
+    total = sum(times)
+    value = tokens * args.steps / total
+    sample = (f"first {tokens} tokens of the {wl.name} workload per step, full V={wl.V} and "
+              f"D={wl.D}, float64 fwd+bwd (loss, lse, dH, dW)")
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(wl, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(wl, world) -> dict:
+    return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens (B=2,S=4096), D={wl.D}, V={wl.V}, "
+                        f"labels {wl.labels}, {int(round(wl.p_ignore * 100))}% ignore_index=-100",
+            "N": wl.N, "D": wl.D, "V": wl.V, "global_batch_tokens": wl.N * world,
+            "l2": "inputs larger than L2 (W alone is %.2f GB > 129 MB)" % (wl.V * wl.D * 2 / 1e9),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(flce_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=1024,
+                    help="tokens in the CPU-oracle baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=256,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    wl = flce_inputs.get(args.workload)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+
+    import torch
+    import linear_cross_entropy_flce_gb300 as flce
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rep = Replicas(world, rank)
+    peaks = load_peaks()
+
+    # Inputs: seeded host draw, pinned host copy (e2e) and device copy (resident).
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H_host = torch.from_numpy(Hb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_host = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.from_numpy(y).pin_memory()
+    H = H_host.to(dev)
+    W = W_host.to(dev)
+    lab = y_host.to(dev)
+    N, D, V = wl.N, wl.D, wl.V
+
+    opts = flce.make_options()
+    plan = flce.get_plan(N, D, V, opts)
+    ws_bytes = flce.workspace_size(N, D, V, opts)
+    out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+           "lse": torch.empty(N, dtype=torch.float32, device=dev),
+           "dH": torch.empty(N, D, dtype=torch.bfloat16, device=dev),
+           "dW": torch.empty(V, D, dtype=torch.float32, device=dev)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # Peak extra device memory of a call, seen by the caching allocator: inputs
+    # and outputs already exist, the library allocates nothing itself, so the
+    # growth is the workspace the caller hands it.
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step():
+        flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
+                              stream=stream.cuda_stream)
+
+    def fwd_step():
+        flce.forward(H, W, lab, out=out, workspace=ws, status=status, stream=stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        step()
+    code = flce.check_status(status, stream.cuda_stream)
+    if code != flce.FLCE_OK:
+        raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
+    peak_delta = torch.cuda.max_memory_allocated(dev) - base
+
+    # ---- device-timed steps (inputs resident) ----
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        rep.barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        rep.barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = rep.max(ms_local)
+    code = flce.check_status(status, stream.cuda_stream)
+    if code != flce.FLCE_OK:
+        raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
+
+    # ---- forward (LSE GEMM) alone, for the per-kernel breakdown ----
+    for _ in range(3):
+        fwd_step()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fwd_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_fwd = ev0.elapsed_time(ev1) / args.steps
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            H.copy_(H_host, non_blocking=True)
+            W.copy_(W_host, non_blocking=True)
+            lab.copy_(y_host, non_blocking=True)
+            step()
+            loss_host.copy_(out["loss"], non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        rep.barrier()
+        t0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = (time.perf_counter() - t0) / args.steps
+        rep.barrier()
+        e2e_ms = rep.max(max(ev0.elapsed_time(ev1) / args.steps, 1e3 * wall))
+        h2d = H_host.numel() * 2 + W_host.numel() * 2 + y_host.numel() * 4
+        e2e = {"value": N * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms}
+
+    flops = 8.0 * N * V * D
+    tflops = flops / (ms / 1e3) / 1e12
+    value = N * world / (ms / 1e3)
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    gemm_launches = plan["kernel_launches"] - 2
+    roofline = {
+        "bound": "tensor", "unit": "TFLOP/s",
+        "kernel": "flce_gemm_kernel (tcgen05; every GEMM launch of the step)",
+        "achieved": tflops, "peak": peak, "frac": tflops / peak,
+        "peak_kind": f"bf16 sustained cuBLAS, {peaks['source']} (burst {peaks['bf16_tflops']})",
+        "frac_of_burst": tflops / peaks["bf16_tflops"],
+        "launches_per_step": gemm_launches,
+        "flops_per_launch_avg": flops / gemm_launches,
+        "note": "step time includes the two small merge/reduce kernels and launch gaps",
+        "traffic": None,
+        "lse_gemm": {"achieved": 2.0 * N * V * D / (ms_fwd / 1e3) / 1e12, "ms": ms_fwd,
+                     "note": "flce_forward alone: the LSE GEMM launch plus merge/reduce"},
+    }
+    clocks = clk.summary()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = cpu_oracle_sample(wl, args.cpu_tokens)
+        cpu = {"value": r["tokens"] / r["seconds"], "unit": UNIT, "cores": blas_threads(),
+               "kind": "oracle", "seconds": r["seconds"],
+               "sample": f"first {r['tokens']} tokens of the {wl.name} workload, full V={V} "
+                         f"and D={D}, float64 fwd+bwd (loss, lse, dH, dW)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no dataset or weights)",
+        "config": config_block(wl, world),
+        "tflops": tflops, "frac_bf16_peak": tflops / peak,
+        "peak_extra_hbm_bytes": int(peak_delta),
+        "workspace_bytes": ws_bytes, "allocator_peak_delta_bytes": int(peak_delta),
+        "logits_bytes_unfused": N * V * 4,
+        "plan": plan,
+        "gpu_launches": plan["kernel_launches"] * args.steps,
+        "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    rep.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

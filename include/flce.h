@@ -32,8 +32,8 @@
  *     tensor-memory-access engine needs 16-byte row strides).
  *   - Ownership: the caller allocates and frees every buffer, the workspace
  *     included. The library allocates no device memory and keeps no pointer after
- *     a call returns (it caches only host-side descriptors keyed by pointer and
- *     shape).
+ *     a call returns (its tensor-memory-access descriptors are encoded on the host
+ *     at each call and passed to the kernels by value).
  *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL means the
  *     legacy default stream) and return before it finishes. Outputs are
  *     overwritten, never accumulated into.
@@ -87,6 +87,18 @@ typedef struct flce_options {
   int64_t timeout_ns;   /* limit of every device-side pipeline wait; 0 = 2 s */
 } flce_options;
 
+/* The execution plan the library will use for a problem on the current device. */
+typedef struct flce_plan_info {
+  int64_t n_block;           /* tokens per backward block */
+  int64_t v_chunk;           /* vocabulary ids per G chunk */
+  int32_t n_blocks;          /* backward token blocks */
+  int32_t n_chunks;          /* backward vocabulary chunks */
+  int32_t v_splits;          /* forward vocabulary ranges per 128-token block */
+  int32_t kernel_launches;   /* kernels one call launches (the status reset is a memset, not counted) */
+  size_t workspace_bytes;    /* the same value flce_workspace_size() returns */
+  size_t plan_bytes;         /* workspace this plan actually touches on this device */
+} flce_plan_info;
+
 /* Fill *opt with the defaults listed above. */
 void flce_default_options(flce_options* opt);
 
@@ -101,6 +113,17 @@ void flce_default_options(flce_options* opt);
  * fp32 logits. Returns FLCE_OK and writes *bytes, or an error code.
  */
 int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt, size_t* bytes);
+
+/*
+ * Describe the plan for an (N, D, V) problem on the current device: token
+ * blocks and vocabulary chunks of the backward pass, vocabulary ranges of the
+ * forward pass, kernel launches per call, workspace bytes. want_dh / want_dw
+ * (0 or 1) say which gradients the call will request; both 0 describes
+ * flce_forward. Needs a current CUDA device (FLCE_ERR_CUDA / FLCE_ERR_DEVICE
+ * otherwise); launches nothing.
+ */
+int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int32_t want_dh,
+                  int32_t want_dw, flce_plan_info* info);
 
 /*
  * Loss, per-token LSE and both gradients in one call.

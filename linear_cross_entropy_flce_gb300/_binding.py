@@ -51,6 +51,19 @@ class Options(ctypes.Structure):
     ]
 
 
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("n_block", ctypes.c_int64),
+        ("v_chunk", ctypes.c_int64),
+        ("n_blocks", ctypes.c_int32),
+        ("n_chunks", ctypes.c_int32),
+        ("v_splits", ctypes.c_int32),
+        ("kernel_launches", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("plan_bytes", ctypes.c_size_t),
+    ]
+
+
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 lib.flce_default_options.argtypes = [ctypes.POINTER(Options)]
@@ -58,6 +71,9 @@ lib.flce_default_options.restype = None
 lib.flce_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options),
                                     ctypes.POINTER(ctypes.c_size_t)]
 lib.flce_workspace_size.restype = ctypes.c_int
+lib.flce_get_plan.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options), ctypes.c_int32,
+                              ctypes.c_int32, ctypes.POINTER(PlanInfo)]
+lib.flce_get_plan.restype = ctypes.c_int
 lib.flce_forward_backward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Options),
                                       _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_forward_backward.restype = ctypes.c_int
@@ -104,6 +120,17 @@ def workspace_size(N: int, D: int, V: int, opts: Optional[Options] = None) -> in
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_workspace_size")
     return int(out.value)
+
+
+def get_plan(N: int, D: int, V: int, opts: Optional[Options] = None, want_dh: bool = True,
+             want_dw: bool = True) -> dict:
+    """The plan flce_forward_backward uses on the current device (needs a GPU)."""
+    info = PlanInfo()
+    rc = lib.flce_get_plan(N, D, V, ctypes.byref(opts) if opts is not None else None,
+                           int(want_dh), int(want_dw), ctypes.byref(info))
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_get_plan")
+    return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
 
 
 @dataclasses.dataclass

@@ -458,6 +458,38 @@ int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt
   return FLCE_OK;
 }
 
+int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int32_t want_dh,
+                  int32_t want_dw, flce_plan_info* info) {
+  if (info == nullptr) return FLCE_ERR_NULL;
+  flce_options o;
+  flce_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  int rc = flce::check_shape(N, D, V);
+  if (rc != FLCE_OK) return rc;
+  rc = flce::check_options(o);
+  if (rc != FLCE_OK) return rc;
+  size_t ws = 0;
+  rc = flce_workspace_size(N, D, V, &o, &ws);
+  if (rc != FLCE_OK) return rc;
+  int sms = 0;
+  rc = flce::device_info(&sms);
+  if (rc != FLCE_OK) return rc;
+  flce::Plan P;
+  rc = flce::make_plan(N, D, V, o, sms, &P);
+  if (rc != FLCE_OK) return rc;
+  info->n_block = P.n_block;
+  info->v_chunk = P.v_chunk;
+  info->n_blocks = P.n_nblocks;
+  info->n_chunks = P.n_chunks;
+  info->v_splits = P.splits;
+  const int per_chunk = 1 + (want_dh ? 1 : 0) + (want_dw ? 1 : 0);
+  info->kernel_launches =
+      3 + ((want_dh || want_dw) ? P.n_nblocks * P.n_chunks * per_chunk : 0);
+  info->workspace_bytes = ws;
+  info->plan_bytes = P.total;
+  return FLCE_OK;
+}
+
 int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N,
                           int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
                           uint16_t* dH, void* dW, void* workspace, size_t ws_bytes,

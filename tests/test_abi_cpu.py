@@ -21,8 +21,9 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_forward_backward",
-                            "flce_forward", "flce_check_status", "flce_status_string"])
+    assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
+                            "flce_forward_backward", "flce_forward", "flce_check_status",
+                            "flce_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -99,6 +100,14 @@ def test_host_rejections_happen_before_device_work():
     o = flce.make_options()
     o.reduction = 5
     assert _call(opts=o) == flce.FLCE_ERR_OPTION
+
+
+def test_plan_rejections_before_device_query():
+    from linear_cross_entropy_flce_gb300._binding import PlanInfo
+    info = PlanInfo()
+    assert flce.lib.flce_get_plan(64, 128, 1000, None, 1, 1, None) == flce.FLCE_ERR_NULL
+    assert flce.lib.flce_get_plan(0, 128, 1000, None, 1, 1, ctypes.byref(info)) == flce.FLCE_ERR_SHAPE
+    assert flce.lib.flce_get_plan(64, 12, 1000, None, 1, 1, ctypes.byref(info)) == flce.FLCE_ERR_ALIGN
 
 
 def test_status_strings():

@@ -192,3 +192,28 @@ def test_token_permutation_equivariance():
 def test_llama2_like_workload_full_parity():
     Hb, Wb, y = flce_inputs.make_inputs(flce_inputs.get("llama2"))
     _run_and_compare(Hb, Wb, y)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "qwen2_7b", "long_seq"])
+def test_full_size_workload_sampled_parity(name):
+    """Full-size workloads in the default plan (the launch configuration the
+    benchmark times): loss and every token's lse against the oracle, dH on 256
+    sampled tokens and dW on 64 sampled vocabulary ids (frequent labels, uniform
+    picks, V-1)."""
+    wl = flce_inputs.get(name)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    del H, W
+    rows = oracle.sample_rows(y, 256, seed=wl.seed)
+    vids = oracle.sample_vocab(y, wl.V, 64, seed=wl.seed)
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f32(Hb), flce_inputs.bf16_bits_to_f32(Wb), y,
+                      dh_rows=rows, dw_rows=vids)
+    dev = res.lse.device
+    errs = compare(res, ref, dh_rows=torch.from_numpy(rows).to(dev),
+                   dw_rows=torch.from_numpy(vids).to(dev))
+    print(name, errs)
+    assert_within(errs)
+    # no [N, V] buffer: the whole extra device memory is the declared workspace
+    assert flce.workspace_size(wl.N, wl.D, wl.V) < wl.N * wl.V * 4 // 8
