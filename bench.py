@@ -212,7 +212,7 @@ def config_block(wl, world) -> dict:
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llama3_8b", choices=sorted(flce_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
