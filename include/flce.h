@@ -153,6 +153,34 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
                  size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * flce_forward, for callers that cannot allocate device memory at call time and
+ * so cannot pass a workspace: for example a plugin whose host application owns
+ * all device memory and gives it no allocator, or a server that reserved its
+ * memory at start-up so that no call can fail with out-of-memory. The pages
+ * have no counterpart of this entry point; it exists only for such callers.
+ *   - Arguments and results are those of flce_forward without the workspace;
+ *     the caller still passes H, W, labels, loss, lse and status.
+ *   - Scratch is one 32 MiB array in device memory owned by the library. Every
+ *     GPU that loads it keeps it until the process exits. The call allocates
+ *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - Limit: problems whose forward scratch exceeds 32 MiB are rejected with
+ *     FLCE_ERR_WORKSPACE before anything is enqueued. The scratch is about
+ *     20 bytes per token plus 512 * D bytes, so at D = 4096 up to about
+ *     1.5 million tokens fit.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, and it keeps the last call's contents.
+ *     Nothing in it needs clearing between calls, because each call writes every
+ *     scratch word before reading it. Calls whose work overlaps on the GPU (on
+ *     different streams, or from different host threads) race on the array and
+ *     give wrong results: serialise them.
+ */
+int flce_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N,
+                         int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
+                         int32_t* status, void* stream);
+
+/*
  * Synchronise `stream`, read the device status word and return it (FLCE_OK, or
  * the first device error a call recorded). Returns FLCE_ERR_CUDA if the stream
  * reports a CUDA error. status == NULL returns FLCE_OK after the synchronisation.

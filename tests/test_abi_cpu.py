@@ -22,8 +22,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
-                            "flce_forward_backward", "flce_forward", "flce_check_status",
-                            "flce_status_string"])
+                            "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
+                            "flce_check_status", "flce_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
