@@ -269,9 +269,6 @@ def main(argv=None) -> int:
         flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
                               stream=stream.cuda_stream)
 
-    def fwd_step():
-        flce.forward(H, W, lab, out=out, workspace=ws, status=status, stream=stream.cuda_stream)
-
     for _ in range(args.warmup):
         step()
     code = flce.check_status(status, stream.cuda_stream)
@@ -297,63 +294,105 @@ def main(argv=None) -> int:
     if code != flce.FLCE_OK:
         raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
 
-    # ---- forward (LSE GEMM) alone, for the per-kernel breakdown ----
-    for _ in range(3):
-        fwd_step()
+    # ---- per-kernel durations: CUDA events the library records on this stream
+    # before its first kernel and after each kernel of a call ----
+    n_launch = plan["kernel_launches"]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
+    for e in evs:
+        e.record(stream)  # creates the event handles
     torch.cuda.synchronize(dev)
-    ev0.record(stream)
+    kinds = ["lse_gemm", "lse_merge", "loss_reduce"] + \
+        ["grad_gemm", "dw_gemm", "dh_gemm"] * (plan["n_blocks"] * plan["n_chunks"])
+    per_kind = {k: 0.0 for k in kinds}
+    n_kind = {k: 0 for k in kinds}
     for _ in range(args.steps):
-        fwd_step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms_fwd = ev0.elapsed_time(ev1) / args.steps
+        flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
+                              stream=stream.cuda_stream, trace_events=evs)
+        torch.cuda.synchronize(dev)
+        for k in range(n_launch):
+            per_kind[kinds[k]] += evs[k].elapsed_time(evs[k + 1])
+            n_kind[kinds[k]] += 1
+    kernel_ms = {k: per_kind[k] / args.steps for k in per_kind}      # per step
+    kernel_launch_ms = {k: per_kind[k] / max(n_kind[k], 1) for k in per_kind}
 
     # ---- end to end through the public API with host buffers ----
+    # Every step copies its inputs (H, W, labels) from pinned host memory and
+    # reads its loss back. The copies of step i+1 run on a copy stream into the
+    # second of two device input buffers while step i computes.
     e2e = None
     if not args.no_e2e:
-        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+        copy_stream = torch.cuda.Stream(dev)
+        bufs = [(H, W, lab), (torch.empty_like(H), torch.empty_like(W), torch.empty_like(lab))]
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        loss_host = torch.empty(args.steps + args.warmup, dtype=torch.float32).pin_memory()
 
-        def e2e_step():
-            H.copy_(H_host, non_blocking=True)
-            W.copy_(W_host, non_blocking=True)
-            lab.copy_(y_host, non_blocking=True)
-            step()
-            loss_host.copy_(out["loss"], non_blocking=True)
+        def run_e2e(nsteps, slot0):
+            for i in range(nsteps):
+                b = i % 2
+                Hd, Wd, yd = bufs[b]
+                copy_stream.wait_event(consumed[b])      # buffer b no longer in use
+                with torch.cuda.stream(copy_stream):
+                    Hd.copy_(H_host, non_blocking=True)
+                    Wd.copy_(W_host, non_blocking=True)
+                    yd.copy_(y_host, non_blocking=True)
+                copied[b].record(copy_stream)
+                stream.wait_event(copied[b])
+                flce.forward_backward(Hd, Wd, yd, out=out, workspace=ws, status=status,
+                                      stream=stream.cuda_stream)
+                consumed[b].record(stream)
+                loss_host[slot0 + i:slot0 + i + 1].copy_(out["loss"], non_blocking=True)
 
-        for _ in range(args.warmup):
-            e2e_step()
+        run_e2e(args.warmup, 0)
         torch.cuda.synchronize(dev)
         rep.barrier()
         t0 = time.perf_counter()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        ev0.record(copy_stream)
+        run_e2e(args.steps, args.warmup)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         wall = (time.perf_counter() - t0) / args.steps
         rep.barrier()
+        code = flce.check_status(status, stream.cuda_stream)
+        if code != flce.FLCE_OK:
+            raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
         e2e_ms = rep.max(max(ev0.elapsed_time(ev1) / args.steps, 1e3 * wall))
         h2d = H_host.numel() * 2 + W_host.numel() * 2 + y_host.numel() * 4
         e2e = {"value": N * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms,
+               "overlap": "copies of step i+1 on a second stream during step i"}
+        del bufs
 
     flops = 8.0 * N * V * D
     tflops = flops / (ms / 1e3) / 1e12
     value = N * world / (ms / 1e3)
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    gemm_launches = plan["kernel_launches"] - 2
+    gemm_flops = 2.0 * N * V * D   # per step, for each of the four products
+
+    def rate(ms_per_step):
+        return gemm_flops / (ms_per_step / 1e3) / 1e12 if ms_per_step > 0 else None
+
+    # The dominant kernel: the tcgen05 GEMM with the fp32 epilogue (dW = G^T H and
+    # dH = G W launches), half of the step's flops and the largest time share.
+    f32_ms = kernel_ms["dw_gemm"] + kernel_ms["dh_gemm"]
+    f32_launches = n_kind["dw_gemm"] + n_kind["dh_gemm"]
+    achieved = 2.0 * gemm_flops / (f32_ms / 1e3) / 1e12
     roofline = {
         "bound": "tensor", "unit": "TFLOP/s",
-        "kernel": "flce_gemm_kernel (tcgen05; every GEMM launch of the step)",
-        "achieved": tflops, "peak": peak, "frac": tflops / peak,
-        "peak_kind": f"bf16 sustained cuBLAS, {peaks['source']} (burst {peaks['bf16_tflops']})",
-        "frac_of_burst": tflops / peaks["bf16_tflops"],
-        "launches_per_step": gemm_launches,
-        "flops_per_launch_avg": flops / gemm_launches,
-        "note": "step time includes the two small merge/reduce kernels and launch gaps",
+        "kernel": "flce_gemm_kernel<EPI_F32> (tcgen05: dW = G^T H and dH = G W launches)",
+        "achieved": achieved, "peak": peak, "frac": achieved / peak,
+        "peak_kind": f"bf16 cuBLAS sustained, {peaks['source']} (burst {peaks['bf16_tflops']})",
+        "frac_of_burst": achieved / peaks["bf16_tflops"],
+        "launches_per_step": f32_launches // args.steps,
+        "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / args.steps),
+        "ms_per_launch_avg": (per_kind["dw_gemm"] + per_kind["dh_gemm"]) / max(f32_launches, 1),
         "traffic": None,
-        "lse_gemm": {"achieved": 2.0 * N * V * D / (ms_fwd / 1e3) / 1e12, "ms": ms_fwd,
-                     "note": "flce_forward alone: the LSE GEMM launch plus merge/reduce"},
+        "kernels": {k: {"ms_per_step": kernel_ms[k], "ms_per_launch": kernel_launch_ms[k],
+                        "launches_per_step": n_kind[k] // args.steps,
+                        "tflops": rate(kernel_ms[k]) if k.endswith("gemm") else None,
+                        "share": kernel_ms[k] / sum(kernel_ms.values())}
+                    for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dw_gemm",
+                              "dh_gemm"]},
     }
     clocks = clk.summary()
 

@@ -85,6 +85,12 @@ typedef struct flce_options {
   int64_t n_block;      /* backward: tokens per block (multiple of 128); 0 = planned */
   int64_t v_chunk;      /* backward: vocabulary ids per G chunk (multiple of 256); 0 = planned */
   int64_t timeout_ns;   /* limit of every device-side pipeline wait; 0 = 2 s */
+  void* const* trace_events; /* optional array of caller-created cudaEvent_t: event 0 is
+                                recorded on `stream` before the first kernel of a call and
+                                event k after its k-th kernel (k <= trace_capacity - 1), so
+                                that kernel k lasts elapsed(event k-1, event k); NULL = off */
+  int32_t trace_capacity;    /* number of events in trace_events */
+  int32_t reserved;          /* must be 0 */
 } flce_options;
 
 /* The execution plan the library will use for a problem on the current device. */

@@ -48,6 +48,9 @@ class Options(ctypes.Structure):
         ("n_block", ctypes.c_int64),
         ("v_chunk", ctypes.c_int64),
         ("timeout_ns", ctypes.c_int64),
+        ("trace_events", ctypes.c_void_p),
+        ("trace_capacity", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -98,7 +101,11 @@ def status_string(code: int) -> str:
 
 def make_options(*, ignore_index: int = -100, reduction: str = "mean", grad_scale: float = 1.0,
                  normalizer: float = 0.0, dw_dtype: str = "float32", v_splits: int = 0,
-                 n_block: int = 0, v_chunk: int = 0, timeout_ns: int = 0) -> Options:
+                 n_block: int = 0, v_chunk: int = 0, timeout_ns: int = 0,
+                 trace_events=None) -> Options:
+    """trace_events: optional sequence of torch.cuda.Event (or raw cudaEvent_t
+    integers); the library records event 0 before its first kernel and event k
+    after its k-th kernel."""
     o = Options()
     lib.flce_default_options(ctypes.byref(o))
     o.ignore_index = int(ignore_index)
@@ -110,6 +117,12 @@ def make_options(*, ignore_index: int = -100, reduction: str = "mean", grad_scal
     o.n_block = int(n_block)
     o.v_chunk = int(v_chunk)
     o.timeout_ns = int(timeout_ns)
+    if trace_events is not None:
+        handles = [int(getattr(e, "cuda_event", e)) for e in trace_events]
+        arr = (ctypes.c_void_p * len(handles))(*handles)
+        o._trace_keepalive = arr
+        o.trace_events = ctypes.cast(arr, ctypes.c_void_p)
+        o.trace_capacity = len(handles)
     return o
 
 

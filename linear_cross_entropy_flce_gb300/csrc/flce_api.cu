@@ -206,6 +206,9 @@ int check_options(const flce_options& o) {
   if (o.dw_dtype != FLCE_DTYPE_F32 && o.dw_dtype != FLCE_DTYPE_BF16) return FLCE_ERR_OPTION;
   if (!(o.normalizer >= 0.f) || !(o.grad_scale == o.grad_scale)) return FLCE_ERR_OPTION;
   if (o.timeout_ns < 0) return FLCE_ERR_OPTION;
+  if (o.trace_capacity < 0 || (o.trace_capacity > 0 && o.trace_events == nullptr) ||
+      o.reserved != 0)
+    return FLCE_ERR_OPTION;
   return FLCE_OK;
 }
 
@@ -263,6 +266,16 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
 
   if (status != nullptr && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess)
     return FLCE_ERR_CUDA;
+  // Optional per-kernel trace: event 0 before the first kernel, event k after kernel k.
+  int n_traced = 0;
+  auto trace = [&]() -> bool {
+    if (o.trace_events == nullptr || n_traced >= o.trace_capacity) return true;
+    const bool ok = cudaEventRecord(static_cast<cudaEvent_t>(o.trace_events[n_traced]), st) ==
+                    cudaSuccess;
+    ++n_traced;
+    return ok;
+  };
+  if (!trace()) return FLCE_ERR_CUDA;
 
   CUtensorMap mH_k, mW_k;
   if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) || !encode_bf16(&mW_k, W, D, V, D, BK, BN))
@@ -289,16 +302,18 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   g.ignore_index = o.ignore_index;
   g.part = part;
   g.zt = zt;
-  if (launch_gemm_lse(mH_k, mW_k, g, std::min(g.num_units, sms), st) != cudaSuccess)
+  if (launch_gemm_lse(mH_k, mW_k, g, std::min(g.num_units, sms), st) != cudaSuccess || !trace())
     return FLCE_ERR_CUDA;
 
   // ---- 2./3. merge and reduce ----
   if (launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V), P.m_blocks,
-                       P.splits, o.ignore_index, lse, nll, st) != cudaSuccess)
+                       P.splits, o.ignore_index, lse, nll, st) != cudaSuccess ||
+      !trace())
     return FLCE_ERR_CUDA;
   if (launch_loss_reduce(nll, labels, static_cast<int>(N), static_cast<int>(V), o.ignore_index,
                          o.reduction, o.grad_scale, o.normalizer, loss, scal, nvalid, status,
-                         st) != cudaSuccess)
+                         st) != cudaSuccess ||
+      !trace())
     return FLCE_ERR_CUDA;
   if (dH == nullptr && dW == nullptr) return FLCE_OK;
 
@@ -342,7 +357,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       q.scale = scal;
       q.g_out = G;
       q.g_ld = P.v_chunk;
-      if (launch_gemm_grad(mH_k, mW_k, q, std::min(q.num_units, sms), st) != cudaSuccess)
+      if (launch_gemm_grad(mH_k, mW_k, q, std::min(q.num_units, sms), st) != cudaSuccess ||
+          !trace())
         return FLCE_ERR_CUDA;
 
       if (dW != nullptr) {
@@ -381,7 +397,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
           w.out_bf16_row0 = static_cast<int>(c0);
           w.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
         }
-        if (launch_gemm_f32(mG_mn, mH_mn, w, std::min(w.num_units, sms), st) != cudaSuccess)
+        if (launch_gemm_f32(mG_mn, mH_mn, w, std::min(w.num_units, sms), st) != cudaSuccess ||
+            !trace())
           return FLCE_ERR_CUDA;
       }
 
@@ -412,7 +429,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
           h.out_mode = OUT_STORE_BF16;
         else
           h.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
-        if (launch_gemm_f32(mG_k, mW_mn, h, std::min(h.num_units, sms), st) != cudaSuccess)
+        if (launch_gemm_f32(mG_k, mW_mn, h, std::min(h.num_units, sms), st) != cudaSuccess ||
+            !trace())
           return FLCE_ERR_CUDA;
       }
     }

@@ -36,7 +36,8 @@ def test_default_options():
     o = flce.make_options()
     assert (o.ignore_index, o.reduction, o.grad_scale, o.normalizer, o.dw_dtype) == (-100, 0, 1.0, 0.0, 0)
     assert (o.v_splits, o.n_block, o.v_chunk, o.timeout_ns) == (0, 0, 0, 0)
-    assert ctypes.sizeof(flce.Options) == 48
+    assert ctypes.sizeof(flce.Options) == 64
+    assert o.trace_events is None and o.trace_capacity == 0 and o.reserved == 0
 
 
 def test_workspace_is_far_below_logits():
@@ -72,6 +73,8 @@ def test_workspace_size_rejects_bad_shapes(kw, code):
     (dict(v_chunk=300), flce.FLCE_ERR_OPTION),
     (dict(n_block=100), flce.FLCE_ERR_OPTION),
     (dict(timeout_ns=-1), flce.FLCE_ERR_OPTION),
+    (dict(trace_capacity=3), flce.FLCE_ERR_OPTION),
+    (dict(reserved=1), flce.FLCE_ERR_OPTION),
 ])
 def test_workspace_size_rejects_bad_options(opt, code):
     o = flce.make_options()

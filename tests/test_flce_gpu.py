@@ -217,3 +217,14 @@ def test_full_size_workload_sampled_parity(name):
     assert_within(errs)
     # no [N, V] buffer: the whole extra device memory is the declared workspace
     assert flce.workspace_size(wl.N, wl.D, wl.V) < wl.N * wl.V * 4 // 8
+
+
+def test_bounded_wait_timeout_sets_status_and_context_stays_usable():
+    """A 1-ns limit makes the kernels' pipeline waits run out: the call must end
+    (no hang), report FLCE_ERR_TIMEOUT through the status word, and leave the
+    CUDA context usable, so that the next normal call is correct."""
+    Hb, Wb, y = _inputs(128, 64, 256, seed=23)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab, timeout_ns=1)
+    assert flce.check_status(res.status) == flce.FLCE_ERR_TIMEOUT
+    _run_and_compare(Hb, Wb, y)
