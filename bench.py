@@ -43,6 +43,39 @@ METRIC = "FLCE fwd+bwd tokens/s & TFLOP/s vs GB300 BF16 peak; peak extra HBM byt
 UNIT = "tokens/s"
 
 
+KERNEL_SOURCES = ("flce_gemm.cuh", "flce_gemm_params.h", "ptx.cuh")
+
+
+def kernel_source_sha() -> str:
+    """sha256 over the GEMM kernel's sources: a DRAM-traffic figure measured with
+    ncu applies only while these are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "linear_cross_entropy_flce_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/dram_traffic_*.md lines 'traffic kernel=... workload=...
+    bytes_per_launch=... kernel_sha=...'); None when absent or when the kernel
+    sources changed since the counters were taken."""
+    import glob
+    sha = kernel_source_sha()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
+        with open(path) as f:
+            for line in f:
+                if not line.startswith("traffic "):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                if kv.get("kernel") == kernel and kv.get("workload") == workload \
+                        and kv.get("kernel_sha") == sha:
+                    return float(kv["bytes_per_launch"])
+    return None
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -202,7 +235,7 @@ def run_reference(args, wl, world, rank):
 
 
 def config_block(wl, world) -> dict:
-    return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens (B=2,S=4096), D={wl.D}, V={wl.V}, "
+    return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens, D={wl.D}, V={wl.V}, "
                         f"labels {wl.labels}, {int(round(wl.p_ignore * 100))}% ignore_index=-100",
             "N": wl.N, "D": wl.D, "V": wl.V, "global_batch_tokens": wl.N * world,
             "l2": "inputs larger than L2 (W alone is %.2f GB > 129 MB)" % (wl.V * wl.D * 2 / 1e9),
@@ -220,12 +253,19 @@ def main(argv=None) -> int:
                     help="tokens in the CPU-oracle baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=256,
                     help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="override V (smaller profiling cases with the workload's other laws)")
+    ap.add_argument("--v-chunk", type=int, default=0, help="plan override: vocabulary ids per G chunk")
+    ap.add_argument("--n-block", type=int, default=0, help="plan override: tokens per block")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
     wl = flce_inputs.get(args.workload)
+    if args.vocab:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_V{args.vocab}", V=args.vocab)
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
@@ -248,7 +288,8 @@ def main(argv=None) -> int:
     lab = y_host.to(dev)
     N, D, V = wl.N, wl.D, wl.V
 
-    opts = flce.make_options()
+    plan_kw = {"v_chunk": args.v_chunk, "n_block": args.n_block}
+    opts = flce.make_options(**plan_kw)
     plan = flce.get_plan(N, D, V, opts)
     ws_bytes = flce.workspace_size(N, D, V, opts)
     out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
@@ -267,7 +308,7 @@ def main(argv=None) -> int:
 
     def step():
         flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
-                              stream=stream.cuda_stream)
+                              stream=stream.cuda_stream, **plan_kw)
 
     for _ in range(args.warmup):
         step()
@@ -307,7 +348,7 @@ def main(argv=None) -> int:
     n_kind = {k: 0 for k in kinds}
     for _ in range(args.steps):
         flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
-                              stream=stream.cuda_stream, trace_events=evs)
+                              stream=stream.cuda_stream, trace_events=evs, **plan_kw)
         torch.cuda.synchronize(dev)
         for k in range(n_launch):
             per_kind[kinds[k]] += evs[k].elapsed_time(evs[k + 1])
@@ -339,7 +380,7 @@ def main(argv=None) -> int:
                 copied[b].record(copy_stream)
                 stream.wait_event(copied[b])
                 flce.forward_backward(Hd, Wd, yd, out=out, workspace=ws, status=status,
-                                      stream=stream.cuda_stream)
+                                      stream=stream.cuda_stream, **plan_kw)
                 consumed[b].record(stream)
                 loss_host[slot0 + i:slot0 + i + 1].copy_(out["loss"], non_blocking=True)
 
@@ -386,7 +427,10 @@ def main(argv=None) -> int:
         "launches_per_step": f32_launches // args.steps,
         "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / args.steps),
         "ms_per_launch_avg": (per_kind["dw_gemm"] + per_kind["dh_gemm"]) / max(f32_launches, 1),
-        "traffic": None,
+        "traffic": measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name),
+        "traffic_source": "profiles/dram_traffic_*.md (ncu dram__bytes_read.sum + "
+                          "dram__bytes_write.sum per launch; null if the kernel changed)",
+        "kernel_sha": kernel_source_sha(),
         "kernels": {k: {"ms_per_step": kernel_ms[k], "ms_per_launch": kernel_launch_ms[k],
                         "launches_per_step": n_kind[k] // args.steps,
                         "tflops": rate(kernel_ms[k]) if k.endswith("gemm") else None,

@@ -98,9 +98,33 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+// Tiles are computed by cluster pairs (tcgen05 cta_group::2, 256-row tiles).
+constexpr int kCtaGroup = 2;
+
+// MN-major bf16 operand [rows][mn] (mn contiguous, mn % 64 == 0, row stride ld
+// elements) as a 3-D map [mn/64][rows][64] read in boxes of 64 x box_rows x
+// box_chunks with 128-byte swizzle. The view covers exactly the 2-D tensor, so
+// every address it can form lies inside it; rows past the end read as zero.
+bool encode_bf16_mn3(CUtensorMap* m, const void* base, uint64_t mn, uint64_t rows, uint64_t ld,
+                     uint32_t box_rows, uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (fn == nullptr || mn % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, mn / 64};
+  cuuint64_t strides[2] = {ld * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct Plan {
   int64_t N = 0, D = 0, V = 0;
-  int m_blocks = 0;   // ceil(N / BM)
+  int cta = kCtaGroup;  // CTAs per tile
+  int tile_m = BM * kCtaGroup;
+  int m_blocks = 0;     // ceil(N / tile_m): row tiles of the forward pass
+  int part_stride = 0;  // 128-row blocks per vocabulary range in the partials
   int v_tiles = 0;    // ceil(V / BN)
   int splits = 0;     // forward vocabulary ranges per token block
   int64_t n_block = 0, v_chunk = 0;
@@ -131,10 +155,12 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
   p.N = N;
   p.D = D;
   p.V = V;
-  p.m_blocks = static_cast<int>(ceil_div(N, BM));
+  p.m_blocks = static_cast<int>(ceil_div(N, p.tile_m));
+  p.part_stride = p.m_blocks * p.cta;
   p.v_tiles = static_cast<int>(ceil_div(V, BN));
   if (o.v_splits < 0 || o.v_splits > p.v_tiles) return FLCE_ERR_OPTION;
-  p.splits = o.v_splits > 0 ? o.v_splits : choose_splits(p.m_blocks, p.v_tiles, sms);
+  p.splits = o.v_splits > 0 ? o.v_splits
+                            : choose_splits(p.m_blocks, p.v_tiles, std::max(1, sms / p.cta));
 
   const int64_t v_round = ceil_div(V, BN) * BN;
   if (o.v_chunk < 0 || o.n_block < 0) return FLCE_ERR_OPTION;
@@ -180,14 +206,14 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
   p.need_dh_acc = p.n_chunks > 1;
   p.need_dw_acc = (o.dw_dtype == FLCE_DTYPE_BF16) && p.n_nblocks > 1;
 
-  const int64_t rows_b = ceil_div(nb, BM) * BM;
+  const int64_t rows_b = ceil_div(nb, p.tile_m) * p.tile_m;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
     off = align_up(off + bytes, 256);
     return at;
   };
-  p.off_part = take(static_cast<size_t>(p.splits) * p.m_blocks * BM * sizeof(float2));
+  p.off_part = take(static_cast<size_t>(p.splits) * p.part_stride * BM * sizeof(float2));
   p.off_zt = take(static_cast<size_t>(N) * 4);
   p.off_nll = take(static_cast<size_t>(N) * 4);
   p.off_lse = take(static_cast<size_t>(N) * 4);
@@ -277,8 +303,11 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   };
   if (!trace()) return FLCE_ERR_CUDA;
 
+  const int cta = P.cta;
+  const int pairs = std::max(1, sms / cta);
   CUtensorMap mH_k, mW_k;
-  if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) || !encode_bf16(&mW_k, W, D, V, D, BK, BN))
+  if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) ||
+      !encode_bf16(&mW_k, W, D, V, D, BK, static_cast<uint32_t>(BN / cta)))
     return FLCE_ERR_CUDA;
 
   // ---- 1. forward LSE GEMM ----
@@ -289,9 +318,10 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   g.n_blocks = P.v_tiles;
   g.k_blocks = static_cast<int>(ceil_div(D, BK));
   g.splits = P.splits;
+  g.part_stride = P.part_stride;
   g.num_units = P.splits * P.m_blocks;
-  g.group_m = 1;
-  g.idesc = make_idesc_bf16_f32(BM, BN, 0, 0);
+  g.group_m = std::min(P.m_blocks, 16);
+  g.idesc = make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
   g.timeout_ns = tmo;
   g.status = status;
   g.m_valid = static_cast<int>(N);
@@ -302,11 +332,12 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   g.ignore_index = o.ignore_index;
   g.part = part;
   g.zt = zt;
-  if (launch_gemm_lse(mH_k, mW_k, g, std::min(g.num_units, sms), st) != cudaSuccess || !trace())
+  if (launch_gemm_lse(cta, mH_k, mW_k, g, cta * std::min(g.num_units, pairs), st) != cudaSuccess ||
+      !trace())
     return FLCE_ERR_CUDA;
 
   // ---- 2./3. merge and reduce ----
-  if (launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V), P.m_blocks,
+  if (launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V), P.part_stride,
                        P.splits, o.ignore_index, lse, nll, st) != cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;
@@ -318,10 +349,17 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   if (dH == nullptr && dW == nullptr) return FLCE_OK;
 
   // ---- 4. backward, token block outer, vocabulary chunk inner ----
-  const int64_t rows_b = ceil_div(P.n_block, BM) * BM;
+  const int64_t rows_b = ceil_div(P.n_block, P.tile_m) * P.tile_m;
+  // MN-major operands: one 3-D copy per CTA when the MN extent is a multiple of
+  // 64 (always for the G chunk), else 64-wide 2-D boxes.
   CUtensorMap mH_mn, mW_mn, mG_mn, mG_k;
-  if (!encode_bf16(&mH_mn, H, D, N, D, 64, BK) || !encode_bf16(&mW_mn, W, D, V, D, 64, BK) ||
-      !encode_bf16(&mG_mn, G, P.v_chunk, rows_b, P.v_chunk, 64, BK) ||
+  const bool d_box3 = D % 64 == 0;
+  const uint32_t b_chunks = static_cast<uint32_t>(BN / cta / 64);
+  const bool ok_h = d_box3 ? encode_bf16_mn3(&mH_mn, H, D, N, D, BK, b_chunks)
+                           : encode_bf16(&mH_mn, H, D, N, D, 64, BK);
+  const bool ok_w = d_box3 ? encode_bf16_mn3(&mW_mn, W, D, V, D, BK, b_chunks)
+                           : encode_bf16(&mW_mn, W, D, V, D, 64, BK);
+  if (!ok_h || !ok_w || !encode_bf16_mn3(&mG_mn, G, P.v_chunk, rows_b, P.v_chunk, BK, BM / 64) ||
       !encode_bf16(&mG_k, G, P.v_chunk, rows_b, P.v_chunk, BK, BM))
     return FLCE_ERR_CUDA;
   const bool dw_bf16 = o.dw_dtype == FLCE_DTYPE_BF16;
@@ -339,12 +377,12 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       q.b_mn_major = 0;
       q.a_mn0 = static_cast<int>(b0);
       q.b_mn0 = static_cast<int>(c0);
-      q.m_blocks = static_cast<int>(ceil_div(nb_len, BM));
+      q.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
       q.n_blocks = static_cast<int>(ceil_div(c_len, BN));
       q.k_blocks = static_cast<int>(ceil_div(D, BK));
       q.num_units = q.m_blocks * q.n_blocks;
-      q.group_m = q.m_blocks;
-      q.idesc = make_idesc_bf16_f32(BM, BN, 0, 0);
+      q.group_m = std::min(q.m_blocks, 16);
+      q.idesc = make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
       q.timeout_ns = tmo;
       q.status = status;
       q.m_valid = nb_len;
@@ -357,7 +395,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       q.scale = scal;
       q.g_out = G;
       q.g_ld = P.v_chunk;
-      if (launch_gemm_grad(mH_k, mW_k, q, std::min(q.num_units, sms), st) != cudaSuccess ||
+      if (launch_gemm_grad(cta, mH_k, mW_k, q, cta * std::min(q.num_units, pairs), st) !=
+              cudaSuccess ||
           !trace())
         return FLCE_ERR_CUDA;
 
@@ -366,13 +405,15 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
         GemmParams w{};
         w.a_mn_major = 1;
         w.b_mn_major = 1;
+        w.a_box3 = 1;
+        w.b_box3 = d_box3 ? 1 : 0;
         w.b_k0 = static_cast<int>(b0);
-        w.m_blocks = static_cast<int>(ceil_div(c_len, BM));
+        w.m_blocks = static_cast<int>(ceil_div(c_len, P.tile_m));
         w.n_blocks = static_cast<int>(ceil_div(D, BN));
         w.k_blocks = static_cast<int>(ceil_div(nb_len, BK));
         w.num_units = w.m_blocks * w.n_blocks;
-        w.group_m = std::min(w.m_blocks, 16);
-        w.idesc = make_idesc_bf16_f32(BM, BN, 1, 1);
+        w.group_m = std::min(w.m_blocks, 8);
+        w.idesc = make_idesc_bf16_f32(P.tile_m, BN, 1, 1);
         w.timeout_ns = tmo;
         w.status = status;
         w.m_valid = c_len;
@@ -397,7 +438,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
           w.out_bf16_row0 = static_cast<int>(c0);
           w.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
         }
-        if (launch_gemm_f32(mG_mn, mH_mn, w, std::min(w.num_units, sms), st) != cudaSuccess ||
+        if (launch_gemm_f32(cta, mG_mn, mH_mn, w, cta * std::min(w.num_units, pairs), st) !=
+                cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;
       }
@@ -407,13 +449,14 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
         GemmParams h{};
         h.a_mn_major = 0;
         h.b_mn_major = 1;
+        h.b_box3 = d_box3 ? 1 : 0;
         h.b_k0 = static_cast<int>(c0);
-        h.m_blocks = static_cast<int>(ceil_div(nb_len, BM));
+        h.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
         h.n_blocks = static_cast<int>(ceil_div(D, BN));
         h.k_blocks = static_cast<int>(ceil_div(c_len, BK));
         h.num_units = h.m_blocks * h.n_blocks;
-        h.group_m = std::min(h.m_blocks, 16);
-        h.idesc = make_idesc_bf16_f32(BM, BN, 0, 1);
+        h.group_m = std::min(h.m_blocks, 8);
+        h.idesc = make_idesc_bf16_f32(P.tile_m, BN, 0, 1);
         h.timeout_ns = tmo;
         h.status = status;
         h.m_valid = nb_len;
@@ -429,7 +472,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
           h.out_mode = OUT_STORE_BF16;
         else
           h.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
-        if (launch_gemm_f32(mG_k, mW_mn, h, std::min(h.num_units, sms), st) != cudaSuccess ||
+        if (launch_gemm_f32(cta, mG_k, mW_mn, h, cta * std::min(h.num_units, pairs), st) !=
+                cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;
       }

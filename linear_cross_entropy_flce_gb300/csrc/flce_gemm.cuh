@@ -14,15 +14,21 @@
 //   F32  : plain product with an fp32 store, fp32 accumulate, or accumulate then
 //          round to bf16 — used for dW = G^T H and dH = G W (same page, 2.).
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0     : TMA producer (one thread) — streams A/B K-slices into a ring of
-//                shared-memory stages.
-//   warp 1     : TMEM allocator and MMA issuer (one thread) — tcgen05.mma
-//                128 x 256 x 16 steps into one of two TMEM accumulators.
+// CTA layout (192 threads, one CTA per SM). kCta = 1: each CTA computes a
+// 128 x 256 tile. kCta = 2: a cluster pair computes a 256 x 256 tile with
+// tcgen05 cta_group::2 MMAs; each CTA holds its 128 rows of A and 128 of the 256
+// rows of B, and its own 128 x 256 fp32 accumulator rows in TMEM.
+//   warp 0     : TMA producer (one thread of the even CTA of a pair) — streams
+//                A/B K-slices for both CTAs into a ring of shared-memory stages;
+//                all copies complete on the even CTA's barriers.
+//   warp 1     : TMEM allocator (both CTAs) and MMA issuer (one thread of the even
+//                CTA) — tcgen05.mma M x 256 x 16 steps into one of two TMEM
+//                accumulators.
 //   warps 2..5 : epilogue — warp w reads TMEM lanes 32*(w%4) .. +31, so each
-//                thread owns one output row of the 128-row tile.
+//                thread owns one output row of its CTA's 128 rows.
 // Every wait is bounded (see mbar_wait_bounded); on a timeout the CTA records
-// FLCE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+// FLCE_ERR_TIMEOUT, the producer drains the copies it issued, the MMA thread
+// drains its MMAs, and both CTAs free TMEM and exit.
 #pragma once
 
 #include <cmath>
@@ -33,24 +39,29 @@
 
 namespace flce {
 
+// Units are ordered in groups of group_m row tiles; inside a group the column
+// index (EPI_LSE: the vocabulary range) is the outer loop, so the tiles running at
+// the same time share both their A row blocks and their B column blocks.
+// Returns the column index (EPI_LSE: the vocabulary range) of unit u.
 template <int kEpi>
-__device__ __forceinline__ void unit_tiles(const GemmParams& p, int u, int& m_blk, int& n_begin,
-                                           int& n_end) {
+__device__ __forceinline__ int unit_tiles(const GemmParams& p, int u, int& m_blk, int& n_begin,
+                                          int& n_end) {
+  const int n_units_per_row = (kEpi == EPI_LSE) ? p.splits : p.n_blocks;
+  const int per_group = p.group_m * n_units_per_row;
+  const int g = u / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.m_blocks - first_m, p.group_m);
+  const int r = u - g * per_group;
+  const int col = r / gm;
+  m_blk = first_m + (r - col * gm);
   if constexpr (kEpi == EPI_LSE) {
-    const int s = u / p.m_blocks;
-    m_blk = u - s * p.m_blocks;
-    n_begin = static_cast<int>((static_cast<int64_t>(s) * p.n_blocks) / p.splits);
-    n_end = static_cast<int>((static_cast<int64_t>(s + 1) * p.n_blocks) / p.splits);
+    n_begin = static_cast<int>((static_cast<int64_t>(col) * p.n_blocks) / p.splits);
+    n_end = static_cast<int>((static_cast<int64_t>(col + 1) * p.n_blocks) / p.splits);
   } else {
-    const int per_group = p.group_m * p.n_blocks;
-    const int g = u / per_group;
-    const int first_m = g * p.group_m;
-    const int gm = min(p.m_blocks - first_m, p.group_m);
-    const int r = u - g * per_group;
-    n_begin = r / gm;
-    m_blk = first_m + (r - n_begin * gm);
-    n_end = n_begin + 1;
+    n_begin = col;
+    n_end = col + 1;
   }
+  return col;
 }
 
 __device__ __forceinline__ void record_status(int32_t* status, int code) {
@@ -160,20 +171,26 @@ __device__ __forceinline__ void f32_chunk(const float (&v)[32], const GemmParams
 
 // ---- the kernel --------------------------------------------------------------------
 
-template <int kEpi>
+template <int kEpi, int kCta>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using Cfg = TileCfg<kCta>;
+  constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
   // bars: full[kStages] | empty[kStages] | tfull[2] | tempty[2] | drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = (kCta == 2) ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x) / kCta;
+  const int num_pairs = static_cast<int>(gridDim.x) / kCta;
   const uint32_t stage0 = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
@@ -188,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), 4 * kCta);  // four epilogue warps per CTA
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -198,9 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  // Barriers of both CTAs are initialised before either CTA touches the other's.
+  if constexpr (kCta == 2) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_cg<kCta>(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish_cg<kCta>();
   }
   tc_fence_before();
   __syncthreads();
@@ -209,13 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    // ---------------- TMA producer (the even CTA issues every copy of the pair) ------
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const uint64_t pol_a = make_l2_policy(p.a_hint);
+      const uint64_t pol_b = make_l2_policy(p.b_hint);
+      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         int m_blk, n_begin, n_end;
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
@@ -225,25 +247,41 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            const uint32_t sa = stage0 + stage * kStageBytes;
-            const uint32_t sb = sa + kABytes;
+            mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
             const int kx = kb * BK;
-            if (!p.a_mn_major) {
-              tma_load_2d(sa, &tmA, kx + p.a_k0, m_blk * BM + p.a_mn0, fb);
-            } else {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d(sa + j * kMnBoxBytes, &tmA, m_blk * BM + 64 * j + p.a_mn0, kx + p.a_k0,
-                            fb);
-            }
-            if (!p.b_mn_major) {
-              tma_load_2d(sb, &tmB, kx + p.b_k0, n_blk * BN + p.b_mn0, fb);
-            } else {
+            for (int r = 0; r < kCta; ++r) {
+              const uint32_t sa_local = stage0 + stage * Cfg::kStageBytes;
+              const uint32_t sa = (kCta == 2) ? mapa_shared(sa_local, r) : sa_local;
+              const uint32_t sb = sa + Cfg::kABytes;
+              const int am = m_blk * Cfg::kTileM + r * BM;      // first A row of CTA r
+              const int bn = n_blk * BN + r * Cfg::kBRows;      // first B row of CTA r
+              auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
+                if constexpr (kCta == 2) tma_load_2d_pair(dst, map, x, y, fb, pol);
+                else tma_load_2d_hint(dst, map, x, y, fb, pol);
+              };
+              auto load3 = [&](uint32_t dst, const CUtensorMap* map, int y, int z, uint64_t pol) {
+                if constexpr (kCta == 2) tma_load_3d_pair(dst, map, 0, y, z, fb, pol);
+                else tma_load_3d_hint(dst, map, 0, y, z, fb, pol);
+              };
+              if (!p.a_mn_major) {
+                load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
+              } else if (p.a_box3) {
+                load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
+              } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(sb + j * kMnBoxBytes, &tmB, n_blk * BN + 64 * j + p.b_mn0, kx + p.b_k0,
-                            fb);
+                for (int j = 0; j < BM / 64; ++j)
+                  load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
+              }
+              if (!p.b_mn_major) {
+                load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
+              } else if (p.b_box3) {
+                load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
+              } else {
+#pragma unroll
+                for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                  load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+              }
             }
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -258,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
-      // Drain: every load this thread issued must land before the CTA exits.
+      // Drain: every copy this thread issued (into either CTA) lands before the
+      // pair passes its final cluster barrier.
       const volatile int no_abort = 0;
       for (int s = 0; s < kStages; ++s)
         if (issued_mask & (1u << s))
@@ -266,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (even CTA) ----------------
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -275,11 +314,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool issued_any = false;
       const bool a_mn = p.a_mn_major != 0, b_mn = p.b_mn_major != 0;
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         int m_blk, n_begin, n_end;
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
-          if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag)) {
+          // both CTAs' epilogues must have drained this accumulator
+          bool got;
+          if constexpr (kCta == 2) {
+            got = mbar_try_wait_cluster(tempty_bar(acc), acc_phase ^ 1u);
+            if (!got) {
+              const uint64_t t0 = global_timer_ns();
+              while (!(got = mbar_try_wait_cluster(tempty_bar(acc), acc_phase ^ 1u))) {
+                if (*abort_flag || global_timer_ns() - t0 > tmo) break;
+              }
+            }
+          } else {
+            got = mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag);
+          }
+          if (!got) {
             ok = false;
             break;
           }
@@ -291,25 +343,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sa = stage0 + stage * kStageBytes;
-            const uint32_t sb = sa + kABytes;
+            const uint32_t sa = stage0 + stage * Cfg::kStageBytes;
+            const uint32_t sb = sa + Cfg::kABytes;
 #pragma unroll
             for (int k = 0; k < BK / UK; ++k) {
               const uint64_t da = a_mn ? make_sw128_desc(sa + k * (UK * 128), kMnBoxBytes, 1024)
                                        : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
               const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
                                        : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
-              umma_bf16(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
+              umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
             }
             issued_any = true;
-            umma_commit(empty_bar(stage));
+            umma_commit_cg<kCta>(empty_bar(stage));
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(tfull_bar(acc));
+          umma_commit_pair<kCta>(tfull_bar(acc));
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -323,25 +375,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued_any) {
         // Drain: all MMAs of this thread complete before TMEM is freed.
         const volatile int no_abort = 0;
-        umma_commit(drain_bar);
+        umma_commit_cg<kCta>(drain_bar);
         mbar_wait_bounded(drain_bar, 0, 1000000000ull, &no_abort);
       }
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps ----------------
+    // ---------------- epilogue warps (both CTAs) ----------------
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // row within the tile
+    const int row = quarter * 32 + lane;  // row within this CTA's 128 rows
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tempty_leader0 = (kCta == 2) ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    const uint32_t tempty_leader1 = (kCta == 2) ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     float scale_v = 0.f;
     if constexpr (kEpi == EPI_GRAD) scale_v = *p.scale;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    for (int u = pair; ok && u < p.num_units; u += num_pairs) {
       int m_blk, n_begin, n_end;
-      unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
-      const int prow = m_blk * BM + row;  // row of the product
+      const int col_unit = unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+      const int prow = m_blk * Cfg::kTileM + static_cast<int>(rank) * BM + row;  // product row
       const bool row_ok = prow < p.m_valid;
       int y = -1;
       if constexpr (kEpi != EPI_F32) {
@@ -351,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       LseState st{-INFINITY, 0.f, 0.f, false};
-      float nlse2 = 0.f, sc = 0.f;
+      // Rows past the product (or of another token block) get exponent -inf, so
+      // their G is exactly 0 whatever logits the tile holds for them.
+      float nlse2 = -INFINITY, sc = 0.f;
       if constexpr (kEpi == EPI_GRAD) {
         if (row_ok) {
           nlse2 = -p.lse[p.row_base + prow] * kLog2e;
@@ -360,7 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int n_blk = n_begin; n_blk < n_end; ++n_blk) {
         int got = 0;
-        if (lane == 0) got = mbar_wait_bounded(tfull_bar(acc), acc_phase, tmo, abort_flag) ? 1 : 0;
+        if (lane == 0) {
+          if constexpr (kCta == 2) {
+            got = mbar_try_wait_cluster(tfull_bar(acc), acc_phase);
+            if (!got) {
+              const uint64_t t0 = global_timer_ns();
+              while (!(got = mbar_try_wait_cluster(tfull_bar(acc), acc_phase))) {
+                if (*abort_flag || global_timer_ns() - t0 > tmo) break;
+              }
+            }
+          } else {
+            got = mbar_wait_bounded(tfull_bar(acc), acc_phase, tmo, abort_flag) ? 1 : 0;
+          }
+        }
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
@@ -388,7 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        if (lane == 0) {
+          if constexpr (kCta == 2) mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+          else mbar_arrive(tempty_bar(acc));
+        }
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -396,7 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (kEpi == EPI_LSE) {
         if (ok) {
-          p.part[static_cast<int64_t>(u) * BM + row] = make_float2(st.m, st.s);
+          // partial slot of (vocabulary range, 128-row block), independent of the raster
+          const int blk128 = m_blk * kCta + static_cast<int>(rank);
+          p.part[(static_cast<int64_t>(col_unit) * p.part_stride + blk128) * BM + row] =
+              make_float2(st.m, st.s);
           if (row_ok && st.found) p.zt[p.row_base + prow] = st.zt;
         }
       }
@@ -408,9 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kCta == 2) cluster_sync();  // the pair's copies and MMAs have drained
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc_cg<kCta>(tmem_base, kTmemCols);
 }
 
 }  // namespace flce

@@ -9,18 +9,29 @@
 
 namespace flce {
 
-constexpr int BM = 128;  // tile rows (tokens, or vocabulary ids for dW)
+constexpr int BM = 128;  // tile rows held by one CTA (tokens, or vocabulary ids for dW)
 constexpr int BN = 256;  // tile columns
 constexpr int BK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UK = 16;   // K per tcgen05.mma for 16-bit inputs
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
-constexpr uint32_t kABytes = BM * BK * 2;
-constexpr uint32_t kBBytes = BN * BK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators
+constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators of BN fp32 columns
 constexpr uint32_t kMnBoxBytes = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major box
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+// Tile configuration. kCta = 1: one CTA computes a 128 x 256 tile. kCta = 2: a
+// cluster pair computes a 256 x 256 tile with tcgen05 cta_group::2; each CTA holds
+// its 128 rows of A and half (128 rows) of B, so each SM stages 32 KB per K step
+// instead of 48 KB, and the ring has 6 stages instead of 4.
+template <int kCta>
+struct TileCfg {
+  static constexpr int kStages = kCta == 2 ? 6 : 4;
+  static constexpr int kTileM = BM * kCta;         // rows of the tile (both CTAs)
+  static constexpr int kBRows = BN / kCta;         // rows of B (tile columns) per CTA
+  static constexpr uint32_t kABytes = BM * BK * 2;
+  static constexpr uint32_t kBBytes = kBRows * BK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // per CTA
+  static constexpr uint32_t kTxBytes = kCta * kStageBytes;    // lands per stage on the pair
+  static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+};
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -44,11 +55,17 @@ struct GemmParams {
   //   K-major  operand: x = k*BK + k0,         y = mn*BLOCK + mn0
   //   MN-major operand: x = mn*BLOCK + 64j + mn0, y = k*BK + k0
   int a_mn_major, b_mn_major;
+  // MN-major operand given as a 3-D map [MN/64][K][64] (MN extent a multiple of 64):
+  // one copy per CTA fills all of its 64-wide chunks; coordinate z = mn / 64.
+  int a_box3, b_box3;
   int a_mn0, a_k0, b_mn0, b_k0;
-  int m_blocks, n_blocks, k_blocks;
+  int m_blocks, n_blocks, k_blocks;  // m_blocks counts tiles of TileCfg::kTileM rows
   int num_units;
-  int splits;   // EPI_LSE: vocabulary ranges; unit u = s * m_blocks + m
-  int group_m;  // other epilogues: tile raster, groups of group_m row blocks
+  int splits;   // EPI_LSE: vocabulary ranges per row block
+  int part_stride;  // EPI_LSE: 128-row blocks per vocabulary range in `part`
+  int group_m;  // tile raster: groups of group_m row blocks (EPI_LSE: units of a group
+                // walk the vocabulary ranges together)
+  int a_hint, b_hint;  // L2 policy of the A / B loads: 0 none, 1 evict_first, 2 evict_last
   uint32_t idesc;
   int64_t timeout_ns;
   int32_t* status;
@@ -59,7 +76,7 @@ struct GemmParams {
   int row_base;
   int col_base;           // vocabulary id of product column 0
   int ignore_index;
-  float2* part;           // EPI_LSE: [num_units][BM] (max, sum exp)
+  float2* part;           // EPI_LSE: [splits][part_stride][BM] (max, sum exp)
   float* zt;              // EPI_LSE: target logit per token
   const float* lse;       // EPI_GRAD: lse[row_base + row]
   const float* scale;     // EPI_GRAD: device scalar grad_scale / n

@@ -11,17 +11,19 @@
 
 namespace flce {
 
-cudaError_t launch_gemm_lse(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                            int grid, cudaStream_t stream);
-cudaError_t launch_gemm_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                             int grid, cudaStream_t stream);
-cudaError_t launch_gemm_f32(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                            int grid, cudaStream_t stream);
+// cta_group 1: grid CTAs of one; cta_group 2: grid/2 clusters of two CTAs.
+cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
+                             const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t stream);
 
 // Per-token merge of the vocabulary-range partials into lse and the per-token
 // negative log-likelihood.
+// part is [splits][part_stride][128] (max, sum exp) pairs.
 cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
-                             int V, int m_blocks, int splits, int ignore_index, float* lse,
+                             int V, int part_stride, int splits, int ignore_index, float* lse,
                              float* nll, cudaStream_t stream);
 
 // One-block deterministic reduction: label validation, n_valid, the loss and

@@ -22,17 +22,17 @@ __device__ __forceinline__ float ex2f_approx(float x) {
 }
 
 __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
-                                 const int32_t* __restrict__ labels, int N, int V, int m_blocks,
+                                 const int32_t* __restrict__ labels, int N, int V, int part_stride,
                                  int splits, int ignore_index, float* __restrict__ lse,
                                  float* __restrict__ nll) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int r = i / BM, l = i - (i / BM) * BM;
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[(static_cast<int64_t>(s) * m_blocks + r) * BM + l].x);
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[(static_cast<int64_t>(s) * part_stride + r) * BM + l].x);
   float S = 0.f;
   for (int s = 0; s < splits; ++s) {
-    const float2 pr = part[(static_cast<int64_t>(s) * m_blocks + r) * BM + l];
+    const float2 pr = part[(static_cast<int64_t>(s) * part_stride + r) * BM + l];
     S += pr.y * ex2f_approx((pr.x - M) * kLog2e);
   }
   const float L = M + logf(S);
@@ -102,11 +102,11 @@ __global__ void __launch_bounds__(kReduceThreads)
 }  // namespace
 
 cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
-                             int V, int m_blocks, int splits, int ignore_index, float* lse,
+                             int V, int part_stride, int splits, int ignore_index, float* lse,
                              float* nll, cudaStream_t stream) {
   const int threads = 256;
   lse_merge_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(
-      part, zt, labels, N, V, m_blocks, splits, ignore_index, lse, nll);
+      part, zt, labels, N, V, part_stride, splits, ignore_index, lse, nll);
   return cudaGetLastError();
 }
 
