@@ -234,6 +234,58 @@ def run_reference(args, wl, world, rank):
     return 0
 
 
+def run_forward_only(args, wl, world, rank, local):
+    """The evaluation path: flce_forward (LSE GEMM, merge, reduce), 2*N*V*D flops."""
+    import torch
+    import linear_cross_entropy_flce_gb300 as flce
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rep = Replicas(world, rank)
+    peaks = load_peaks()
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H = torch.from_numpy(Hb.view(np.int16)).to(dev).view(torch.bfloat16)
+    W = torch.from_numpy(Wb.view(np.int16)).to(dev).view(torch.bfloat16)
+    lab = torch.from_numpy(y).to(dev)
+    N, D, V = wl.N, wl.D, wl.V
+    ws = torch.empty(flce.workspace_size(N, D, V), dtype=torch.uint8, device=dev)
+    out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+           "lse": torch.empty(N, dtype=torch.float32, device=dev)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        flce.forward(H, W, lab, out=out, workspace=ws, status=status, stream=stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        step()
+    if flce.check_status(status, stream.cuda_stream) != flce.FLCE_OK:
+        raise RuntimeError("device status error")
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        rep.barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        rep.barrier()
+    ms = rep.max(ev0.elapsed_time(ev1) / args.steps)
+    tflops = 2.0 * N * V * D / (ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    line = {"metric": "FLCE forward (loss + lse) tokens/s", "value": N * world / (ms / 1e3),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; no dataset or weights)",
+            "config": config_block(wl, world), "tflops": tflops, "frac_bf16_peak": tflops / peak,
+            "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    rep.close()
+    return 0
+
+
 def config_block(wl, world) -> dict:
     return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens, D={wl.D}, V={wl.V}, "
                         f"labels {wl.labels}, {int(round(wl.p_ignore * 100))}% ignore_index=-100",
@@ -257,6 +309,8 @@ def main(argv=None) -> int:
                     help="override V (smaller profiling cases with the workload's other laws)")
     ap.add_argument("--v-chunk", type=int, default=0, help="plan override: vocabulary ids per G chunk")
     ap.add_argument("--n-block", type=int, default=0, help="plan override: tokens per block")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time flce_forward (loss and lse, the evaluation path) instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
@@ -269,6 +323,8 @@ def main(argv=None) -> int:
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
+    if args.forward_only:
+        return run_forward_only(args, wl, world, rank, local)
 
     import torch
     import linear_cross_entropy_flce_gb300 as flce

@@ -71,12 +71,14 @@ enum {
   FLCE_ERR_TIMEOUT = 9      /* device: a pipeline wait exceeded timeout_ns */
 };
 
-enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 };
+/* FLCE_REDUCTION_NONE (per-token loss) is accepted by flce_forward and
+ * flce_forward_noalloc only; flce_forward_backward rejects it with FLCE_ERR_OPTION. */
+enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1, FLCE_REDUCTION_NONE = 2 };
 enum { FLCE_DTYPE_F32 = 0, FLCE_DTYPE_BF16 = 1 };
 
 typedef struct flce_options {
   int32_t ignore_index; /* label value that marks an ignored token; default -100 */
-  int32_t reduction;    /* FLCE_REDUCTION_MEAN (default) or FLCE_REDUCTION_SUM */
+  int32_t reduction;    /* FLCE_REDUCTION_MEAN (default), _SUM, or _NONE (forward only) */
   float grad_scale;     /* upstream dL/dloss multiplying G; default 1 */
   float normalizer;     /* > 0: mean divides by this instead of the device-counted n
                            (a global token count for data-parallel callers); default 0 */
@@ -151,8 +153,11 @@ int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* l
                           int32_t* status, void* stream);
 
 /*
- * Forward only: the loss and (optionally) lse, without any gradient work. Same
- * arguments and rules as flce_forward_backward.
+ * Forward only: the loss and (optionally) lse, without any gradient work (the
+ * evaluation path). Same arguments and rules as flce_forward_backward, except
+ * that with reduction FLCE_REDUCTION_NONE `loss` is fp32 [N]: each token's
+ * lse_i - z_{i,y_i}, and 0 for ignored tokens (the per-token loss of PyTorch's
+ * reduction="none").
  */
 int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
                  int64_t V, const flce_options* opt, float* loss, float* lse, void* workspace,
@@ -185,6 +190,30 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
 int flce_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N,
                          int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
                          int32_t* status, void* stream);
+
+/*
+ * Cross-entropy over a given logits matrix: the unfused loss that fused linear
+ * cross-entropy replaces (GPU MODE lecture 28 notes, cross-entropy section:
+ * LigerCrossEntropyLoss(reduction="mean")(logits.view(-1, vocab), labels)).
+ * Same loss, lse, ignore and scaling rules as flce_forward_backward, with z
+ * given directly:
+ *   logits   [N, V] fp32 or bf16 (dtype = FLCE_DTYPE_F32 / FLCE_DTYPE_BF16), row
+ *            stride ld elements (ld >= V; ld * element size a multiple of 16)
+ *   loss     fp32 [1], or fp32 [N] per-token losses with FLCE_REDUCTION_NONE
+ *   lse      fp32 [N] (may be NULL)
+ *   dlogits  [N, V] of the same dtype, row stride dld (may be NULL: no gradient;
+ *            may equal logits with dld == ld: the gradient overwrites the logits
+ *            row by row; must not otherwise overlap them). Not allowed with
+ *            FLCE_REDUCTION_NONE.
+ *   workspace of flce_ce_workspace_size() bytes (per-token loss, lse, scalars).
+ * One read of the logits for the loss; for the gradient the row is read again
+ * (mostly from L2) and dlogits written once.
+ */
+int flce_ce_workspace_size(int64_t N, int64_t V, const flce_options* opt, size_t* bytes);
+int flce_ce_logits(const void* logits, int32_t dtype, int64_t ld, const int32_t* labels,
+                   int64_t N, int64_t V, const flce_options* opt, float* loss, float* lse,
+                   void* dlogits, int64_t dld, void* workspace, size_t ws_bytes, int32_t* status,
+                   void* stream);
 
 /*
  * Synchronise `stream`, read the device status word and return it (FLCE_OK, or

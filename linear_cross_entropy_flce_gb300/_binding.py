@@ -33,7 +33,7 @@ FLCE_ERR_DEVICE = 7
 FLCE_ERR_LABEL_RANGE = 8
 FLCE_ERR_TIMEOUT = 9
 
-REDUCTIONS = {"mean": 0, "sum": 1}
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 DW_DTYPES = {"float32": 0, "bfloat16": 1}
 
 
@@ -83,6 +83,12 @@ lib.flce_forward_backward.restype = ctypes.c_int
 lib.flce_forward.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Options),
                              _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_forward.restype = ctypes.c_int
+lib.flce_ce_workspace_size.argtypes = [_i64, _i64, ctypes.POINTER(Options),
+                                       ctypes.POINTER(ctypes.c_size_t)]
+lib.flce_ce_workspace_size.restype = ctypes.c_int
+lib.flce_ce_logits.argtypes = [_vp, ctypes.c_int32, _i64, _vp, _i64, _i64, ctypes.POINTER(Options),
+                               _vp, _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp, _vp]
+lib.flce_ce_logits.restype = ctypes.c_int
 lib.flce_check_status.argtypes = [_vp, _vp]
 lib.flce_check_status.restype = ctypes.c_int
 lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -224,7 +230,8 @@ def forward_backward(H, W, labels, *, need_dh: bool = True, need_dw: bool = True
 
 def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=None,
             stream=None, **options) -> Result:
-    """Loss and lse only, via flce_forward."""
+    """Loss and lse only, via flce_forward. With reduction="none" the loss is
+    the per-token loss [N] (0 for ignored tokens)."""
     import torch
     N, D, V = _check_inputs(H, W, labels)
     opts = make_options(**options)
@@ -232,7 +239,8 @@ def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=
     out = dict(out or {})
     loss = out.get("loss")
     if loss is None:
-        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        n_loss = N if options.get("reduction") == "none" else 1
+        loss = torch.empty(n_loss, dtype=torch.float32, device=dev)
     lse = out.get("lse")
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
@@ -249,6 +257,57 @@ def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_forward")
     return Result(loss, lse, None, None, status)
+
+
+def ce_logits(logits, labels, *, need_grad: bool = True, in_place: bool = False,
+              out: Optional[dict] = None, workspace=None, status=None, stream=None,
+              **options) -> Result:
+    """Cross-entropy over given logits [N, V] (fp32 or bf16) via flce_ce_logits.
+    Returns Result(loss, lse, dH=None, dW=None) with the gradient in
+    result.dlogits (the logits tensor itself when in_place)."""
+    import torch
+    if not (logits.is_cuda and labels.is_cuda):
+        raise ValueError("logits and labels must be CUDA tensors")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [N, V] with unit column stride")
+    if logits.dtype not in (torch.float32, torch.bfloat16) or labels.dtype != torch.int32:
+        raise TypeError("logits float32/bfloat16, labels int32")
+    N, V = logits.shape
+    ld = logits.stride(0)
+    dtype = 1 if logits.dtype == torch.bfloat16 else 0
+    opts = make_options(**options)
+    dev = logits.device
+    out = dict(out or {})
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(N if options.get("reduction") == "none" else 1, dtype=torch.float32,
+                           device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    grad = None
+    if need_grad:
+        grad = logits if in_place else out.get("dlogits")
+        if grad is None:
+            grad = torch.empty_like(logits)
+    size = ctypes.c_size_t(0)
+    rc = lib.flce_ce_workspace_size(N, V, ctypes.byref(opts), ctypes.byref(size))
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_ce_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(int(size.value), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_ce_logits(_ptr(logits), dtype, ld, _ptr(labels), N, V, ctypes.byref(opts),
+                            _ptr(loss), _ptr(lse), _ptr(grad), grad.stride(0) if grad is not None else 0,
+                            _ptr(workspace), workspace.numel(), _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_ce_logits")
+    r = Result(loss, lse, None, None, status)
+    r.dlogits = grad
+    return r
 
 
 def check_status(status, stream=None) -> int:

@@ -24,7 +24,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", 
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
 
 SOURCES = ["flce_api.cu", "flce_reduce.cu", "flce_gemm_lse.cu", "flce_gemm_grad.cu",
-           "flce_gemm_f32.cu", "flce_noalloc.cu"]
+           "flce_gemm_f32.cu", "flce_noalloc.cu", "flce_ce.cu"]
 
 
 def nvcc() -> str:

@@ -227,7 +227,8 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
 }
 
 int check_options(const flce_options& o) {
-  if (o.reduction != FLCE_REDUCTION_MEAN && o.reduction != FLCE_REDUCTION_SUM)
+  if (o.reduction != FLCE_REDUCTION_MEAN && o.reduction != FLCE_REDUCTION_SUM &&
+      o.reduction != FLCE_REDUCTION_NONE)
     return FLCE_ERR_OPTION;
   if (o.dw_dtype != FLCE_DTYPE_F32 && o.dw_dtype != FLCE_DTYPE_BF16) return FLCE_ERR_OPTION;
   if (!(o.normalizer >= 0.f) || !(o.grad_scale == o.grad_scale)) return FLCE_ERR_OPTION;
@@ -275,13 +276,18 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   if (!backward) {
     dH = nullptr;
     dW = nullptr;
+  } else if (o.reduction == FLCE_REDUCTION_NONE) {
+    return FLCE_ERR_OPTION;  // a per-token loss needs a per-token upstream gradient
   }
+  const bool per_token = o.reduction == FLCE_REDUCTION_NONE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float2* part = reinterpret_cast<float2*>(ws + P.off_part);
   float* zt = reinterpret_cast<float*>(ws + P.off_zt);
-  float* nll = reinterpret_cast<float*>(ws + P.off_nll);
+  // reduction "none": the merge writes each token's loss straight to the caller
+  float* nll = per_token ? loss : reinterpret_cast<float*>(ws + P.off_nll);
+  float* loss_scalar = per_token ? reinterpret_cast<float*>(ws + P.off_scal + 8) : loss;
   float* lse = lse_out ? lse_out : reinterpret_cast<float*>(ws + P.off_lse);
   float* scal = reinterpret_cast<float*>(ws + P.off_scal);  // [0] scale
   int32_t* nvalid = reinterpret_cast<int32_t*>(ws + P.off_scal + 4);
@@ -342,7 +348,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       !trace())
     return FLCE_ERR_CUDA;
   if (launch_loss_reduce(nll, labels, static_cast<int>(N), static_cast<int>(V), o.ignore_index,
-                         o.reduction, o.grad_scale, o.normalizer, loss, scal, nvalid, status,
+                         per_token ? FLCE_REDUCTION_SUM : o.reduction, o.grad_scale,
+                         o.normalizer, loss_scalar, scal, nvalid, status,
                          st) != cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;
@@ -549,6 +556,89 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
       3 + ((want_dh || want_dw) ? P.n_nblocks * P.n_chunks * per_chunk : 0);
   info->workspace_bytes = ws;
   info->plan_bytes = P.total;
+  return FLCE_OK;
+}
+
+int flce_ce_workspace_size(int64_t N, int64_t V, const flce_options* opt, size_t* bytes) {
+  if (bytes == nullptr) return FLCE_ERR_NULL;
+  flce_options o;
+  flce_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  if (N < 1 || V < 1 || N > (int64_t(1) << 30) || V > (int64_t(1) << 30)) return FLCE_ERR_SHAPE;
+  const int rc = flce::check_options(o);
+  if (rc != FLCE_OK) return rc;
+  *bytes = 2 * flce::align_up(static_cast<size_t>(N) * 4, 256) + 256;
+  return FLCE_OK;
+}
+
+int flce_ce_logits(const void* logits, int32_t dtype, int64_t ld, const int32_t* labels,
+                   int64_t N, int64_t V, const flce_options* opt, float* loss, float* lse,
+                   void* dlogits, int64_t dld, void* workspace, size_t ws_bytes, int32_t* status,
+                   void* stream) {
+  flce_options o;
+  flce_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  if (logits == nullptr || labels == nullptr || loss == nullptr || workspace == nullptr)
+    return FLCE_ERR_NULL;
+  if (N < 1 || V < 1 || N > (int64_t(1) << 30) || V > (int64_t(1) << 30)) return FLCE_ERR_SHAPE;
+  int rc = flce::check_options(o);
+  if (rc != FLCE_OK) return rc;
+  if (dtype != FLCE_DTYPE_F32 && dtype != FLCE_DTYPE_BF16) return FLCE_ERR_OPTION;
+  const int64_t elt = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  if (ld < V || (dlogits != nullptr && dld < V)) return FLCE_ERR_SHAPE;
+  if ((ld * elt) % 16 != 0 || (dlogits != nullptr && (dld * elt) % 16 != 0)) return FLCE_ERR_ALIGN;
+  if (!flce::aligned16(logits) || !flce::aligned16(labels) || !flce::aligned16(workspace) ||
+      (dlogits && !flce::aligned16(dlogits)) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(loss) & 3u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return FLCE_ERR_ALIGN;
+  if (dlogits == logits && dld != ld) return FLCE_ERR_OPTION;
+  if (dlogits != nullptr && o.reduction == FLCE_REDUCTION_NONE) return FLCE_ERR_OPTION;
+  size_t need = 0;
+  rc = flce_ce_workspace_size(N, V, &o, &need);
+  if (rc != FLCE_OK) return rc;
+  if (ws_bytes < need) return FLCE_ERR_WORKSPACE;
+  int sms = 0;
+  rc = flce::device_info(&sms);
+  if (rc != FLCE_OK) return rc;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t nb = flce::align_up(static_cast<size_t>(N) * 4, 256);
+  const bool per_token = o.reduction == FLCE_REDUCTION_NONE;
+  float* nll = per_token ? loss : reinterpret_cast<float*>(ws);
+  float* lse_ws = reinterpret_cast<float*>(ws + nb);
+  float* scal = reinterpret_cast<float*>(ws + 2 * nb);
+  int32_t* nvalid = reinterpret_cast<int32_t*>(ws + 2 * nb + 4);
+  float* loss_scalar = per_token ? reinterpret_cast<float*>(ws + 2 * nb + 8) : loss;
+  if (status != nullptr && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  int n_traced = 0;
+  auto trace = [&]() -> bool {
+    if (o.trace_events == nullptr || n_traced >= o.trace_capacity) return true;
+    const bool ok = cudaEventRecord(static_cast<cudaEvent_t>(o.trace_events[n_traced]), st) ==
+                    cudaSuccess;
+    ++n_traced;
+    return ok;
+  };
+  if (!trace()) return FLCE_ERR_CUDA;
+  const int Ni = static_cast<int>(N), Vi = static_cast<int>(V);
+  if (dlogits != nullptr &&
+      (flce::launch_ce_count(labels, Ni, Vi, o.ignore_index, o.reduction, o.grad_scale,
+                             o.normalizer, scal, status, st) != cudaSuccess ||
+       !trace()))
+    return FLCE_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(sms) * 4));
+  if (flce::launch_ce_rows(dtype == FLCE_DTYPE_BF16 ? 1 : 0, logits, ld * elt, labels, Ni, Vi,
+                           o.ignore_index, scal, lse ? lse : lse_ws, nll, dlogits, dld * elt, grid,
+                           st) != cudaSuccess ||
+      !trace())
+    return FLCE_ERR_CUDA;
+  if (flce::launch_loss_reduce(nll, labels, Ni, Vi, o.ignore_index,
+                               per_token ? FLCE_REDUCTION_SUM : o.reduction, o.grad_scale,
+                               o.normalizer, loss_scalar, scal + 3, nvalid, status,
+                               st) != cudaSuccess ||
+      !trace())
+    return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
 

@@ -1,0 +1,273 @@
+// Cross-entropy over a given logits matrix Z [N, V] (fp32 or bf16): the
+// unfused loss that fused linear cross-entropy replaces ("GPU MODE lecture 28"
+// notes, cross-entropy section: the loss takes logits.view(-1, vocab) and labels
+// with reduction="mean"). It is a bandwidth-bound pass: the logits are read
+// once for the online log-sum-exp and, for the gradient, the same row is read
+// again (from L2) and dZ = (softmax - onehot) * scale is written, in place when
+// the caller passes the logits as the gradient buffer.
+//
+// Kernels:
+//   ce_count_kernel : one block; n_valid, label check, gradient scale.
+//   ce_rows_kernel  : persistent CTAs, one row at a time: 16-byte vector loads,
+//                     per-thread running (max, sum exp) merged across the block,
+//                     lse and the per-token loss, then (optionally) the gradient.
+// The loss itself is formed by loss_reduce_kernel (flce_reduce.cu).
+#include <cmath>
+#include <cstdint>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+namespace {
+
+constexpr int kCeThreads = 512;
+constexpr int kCountThreads = 1024;
+
+__device__ __forceinline__ float ex2a(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16-byte vector of logits: 4 fp32 or 8 bf16, widened to fp32.
+template <int kBf16>
+struct Vec16;
+
+template <>
+struct Vec16<0> {
+  static constexpr int E = 4;
+  __device__ static void load(const void* p, float (&x)[4]) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  __device__ static void store(void* p, const float (&x)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  }
+  __device__ static float load1(const void* p) { return __ldcg(reinterpret_cast<const float*>(p)); }
+  __device__ static void store1(void* p, float v) { *reinterpret_cast<float*>(p) = v; }
+};
+
+template <>
+struct Vec16<1> {
+  static constexpr int E = 8;
+  __device__ static void load(const void* p, float (&x)[8]) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p));
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+  }
+  __device__ static void store(void* p, const float (&x)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                              pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+  }
+  __device__ static float load1(const void* p) {
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+  }
+  __device__ static void store1(void* p, float v) {
+    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(pack_bf16(v, 0.f) & 0xFFFFu);
+  }
+};
+
+// (m, s) with s = sum exp(z - m): merge two partial states.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  s = s * ex2a((m - mn) * kLog2e) + s2 * ex2a((m2 - mn) * kLog2e);
+  m = mn;
+}
+
+__global__ void __launch_bounds__(kCountThreads)
+    ce_count_kernel(const int32_t* __restrict__ labels, int N, int V, int ignore_index,
+                    int reduction, float grad_scale, float normalizer, float* scale,
+                    int32_t* status) {
+  __shared__ int s_cnt[kCountThreads];
+  __shared__ int s_bad[kCountThreads];
+  const int t = threadIdx.x;
+  int cnt = 0, bad = 0;
+  for (int i = t; i < N; i += kCountThreads) {
+    const int y = labels[i];
+    if (y == ignore_index) continue;
+    if (y < 0 || y >= V) bad = 1;
+    else ++cnt;
+  }
+  s_cnt[t] = cnt;
+  s_bad[t] = bad;
+  __syncthreads();
+  for (int w = kCountThreads / 2; w > 0; w >>= 1) {
+    if (t < w) {
+      s_cnt[t] += s_cnt[t + w];
+      s_bad[t] |= s_bad[t + w];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    const int n = s_cnt[0];
+    double sc;
+    if (reduction == 1) sc = grad_scale;
+    else if (normalizer > 0.f) sc = grad_scale / static_cast<double>(normalizer);
+    else sc = n > 0 ? grad_scale / static_cast<double>(n) : 0.0;
+    *scale = static_cast<float>(sc);
+    if (s_bad[0] && status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, 8);
+  }
+}
+
+template <int kBf16, bool kGrad>
+__global__ void __launch_bounds__(kCeThreads)
+    ce_rows_kernel(const uint8_t* z, int64_t ld_bytes,  // may alias g (in place)
+                   const int32_t* __restrict__ labels, int N, int V, int ignore_index,
+                   const float* __restrict__ scale_ptr, float* __restrict__ lse_out,
+                   float* __restrict__ nll_out, uint8_t* g, int64_t gld_bytes) {
+  using VT = Vec16<kBf16>;
+  constexpr int E = VT::E;
+  constexpr int kElt = kBf16 ? 2 : 4;
+  constexpr int kUnroll = 4;
+  __shared__ float2 s_red[kCeThreads / 32];
+  __shared__ float s_lse;
+  __shared__ int s_y;  // target id, -1 when the token is ignored
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const float scale = kGrad ? *scale_ptr : 0.f;
+  const int nvec = V / E;
+
+  for (int row = blockIdx.x; row < N; row += gridDim.x) {
+    const uint8_t* zr = z + static_cast<int64_t>(row) * ld_bytes;
+    float m = -INFINITY, s = 0.f;
+    // pass 1: running max and sum of exponentials
+    int v = tid;
+    for (; v + (kUnroll - 1) * kCeThreads < nvec; v += kUnroll * kCeThreads) {
+      float x[kUnroll][E];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        VT::load(zr + static_cast<int64_t>(v + u * kCeThreads) * 16, x[u]);
+      float cm = m;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[u][e]);
+      const float ms = cm * kLog2e;
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc += ex2a(fmaf(x[u][e], kLog2e, -ms));
+      s = s * ex2a((m - cm) * kLog2e) + acc;
+      m = cm;
+    }
+    for (; v < nvec; v += kCeThreads) {
+      float x[E];
+      VT::load(zr + static_cast<int64_t>(v) * 16, x);
+      float cm = m;
+#pragma unroll
+      for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[e]);
+      const float ms = cm * kLog2e;
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc += ex2a(fmaf(x[e], kLog2e, -ms));
+      s = s * ex2a((m - cm) * kLog2e) + acc;
+      m = cm;
+    }
+    for (int i = nvec * E + tid; i < V; i += kCeThreads) {
+      const float x = VT::load1(zr + static_cast<int64_t>(i) * kElt);
+      lse_merge(m, s, x, 1.f);
+    }
+    // block merge: warp shuffles, then the first warp
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    if (lane == 0) s_red[warp] = make_float2(m, s);
+    __syncthreads();
+    if (warp == 0) {
+      float2 r = lane < kCeThreads / 32 ? s_red[lane] : make_float2(-INFINITY, 0.f);
+      m = r.x;
+      s = r.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        lse_merge(m, s, m2, s2);
+      }
+      if (lane == 0) {
+        const float lse = m + logf(s);
+        const int y = labels[row];
+        const bool valid = y != ignore_index && y >= 0 && y < V;
+        const float zt = valid ? VT::load1(zr + static_cast<int64_t>(y) * kElt) : 0.f;
+        if (lse_out != nullptr) lse_out[row] = lse;
+        nll_out[row] = valid ? lse - zt : 0.f;
+        s_lse = lse;
+        s_y = valid ? y : -1;
+      }
+    }
+    __syncthreads();
+    if constexpr (kGrad) {
+      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale, 0 for ignored rows
+      const float lse = s_lse;
+      const int y = s_y;
+      const float sc = y >= 0 ? scale : 0.f;
+      const float nl2 = -lse * kLog2e;
+      uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
+      for (int w = tid; w < nvec; w += kCeThreads) {
+        float x[E];
+        VT::load(zr + static_cast<int64_t>(w) * 16, x);
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
+        const int base = w * E;
+        if (static_cast<unsigned>(y - base) < static_cast<unsigned>(E)) {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (base + e == y) x[e] -= sc;
+        }
+        VT::store(gr + static_cast<int64_t>(w) * 16, x);
+      }
+      for (int i = nvec * E + tid; i < V; i += kCeThreads) {
+        float x = ex2a(fmaf(VT::load1(zr + static_cast<int64_t>(i) * kElt), kLog2e, nl2)) * sc;
+        if (i == y) x -= sc;
+        VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
+      }
+    }
+    __syncthreads();  // s_red, s_lse, s_y reused by the next row
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ce_count(const int32_t* labels, int N, int V, int ignore_index, int reduction,
+                            float grad_scale, float normalizer, float* scale, int32_t* status,
+                            cudaStream_t stream) {
+  ce_count_kernel<<<1, kCountThreads, 0, stream>>>(labels, N, V, ignore_index, reduction,
+                                                   grad_scale, normalizer, scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int32_t* labels,
+                           int N, int V, int ignore_index, const float* scale, float* lse,
+                           float* nll, void* g, int64_t gld_bytes, int grid,
+                           cudaStream_t stream) {
+  const uint8_t* zp = static_cast<const uint8_t*>(z);
+  uint8_t* gp = static_cast<uint8_t*>(g);
+  if (bf16) {
+    if (g) ce_rows_kernel<1, true><<<grid, kCeThreads, 0, stream>>>(
+        zp, ld_bytes, labels, N, V, ignore_index, scale, lse, nll, gp, gld_bytes);
+    else ce_rows_kernel<1, false><<<grid, kCeThreads, 0, stream>>>(
+        zp, ld_bytes, labels, N, V, ignore_index, scale, lse, nll, gp, gld_bytes);
+  } else {
+    if (g) ce_rows_kernel<0, true><<<grid, kCeThreads, 0, stream>>>(
+        zp, ld_bytes, labels, N, V, ignore_index, scale, lse, nll, gp, gld_bytes);
+    else ce_rows_kernel<0, false><<<grid, kCeThreads, 0, stream>>>(
+        zp, ld_bytes, labels, N, V, ignore_index, scale, lse, nll, gp, gld_bytes);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -33,4 +33,15 @@ cudaError_t launch_loss_reduce(const float* nll, const int32_t* labels, int N, i
                                float normalizer, float* loss, float* scale, int32_t* n_valid,
                                int32_t* status, cudaStream_t stream);
 
+// Cross-entropy over given logits: label count and gradient scale (one block),
+// then the row pass (lse, per-token loss, optional gradient; bf16 = 1 for bf16
+// logits and gradient, 0 for fp32). g may equal z (in place, same row stride).
+cudaError_t launch_ce_count(const int32_t* labels, int N, int V, int ignore_index, int reduction,
+                            float grad_scale, float normalizer, float* scale, int32_t* status,
+                            cudaStream_t stream);
+cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int32_t* labels,
+                           int N, int V, int ignore_index, const float* scale, float* lse,
+                           float* nll, void* g, int64_t gld_bytes, int grid,
+                           cudaStream_t stream);
+
 }  // namespace flce

@@ -41,6 +41,9 @@ rows only to bound host memory; blocking does not change any per-row result.
 dW_v is a sum over all tokens; it is computed per block of vocabulary ids,
 each column-block of G over all tokens at once, so no sum over tokens is split.
 
+ce_logits() is the same loss over a given logits matrix (the unfused
+cross-entropy that fused linear cross-entropy replaces).
+
 Parity status: every function here is pinned by tests under tests/ (closed
 forms, brute-force log-sum-exp, finite differences, the pages' printed
 memory figures); none is "parity unpinned".
@@ -168,6 +171,60 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
 
     return dict(loss=loss, lse=lse, nll=nll, n_valid=n_valid, dH=dH, dW=dW,
                 dh_rows=dh_sel, dw_rows=dw_sel)
+
+
+def ce_logits(Z: np.ndarray, labels: np.ndarray, *, ignore_index: int = IGNORE_INDEX,
+              reduction: str = "mean", grad_scale: float = 1.0, normalizer: float = 0.0,
+              want_grad: bool = True, row_block: int = 1024) -> dict:
+    """Cross-entropy over given logits Z [N, V] (the unfused loss the fused one
+    replaces: the cross-entropy section of the GPU MODE lecture 28 notes, which
+    takes logits.view(-1, vocab) and labels with reduction="mean"), float64.
+
+    Same definitions and readings as flce() with z_iv given directly:
+    lse_i = m_i + log sum_v exp(z_iv - m_i), per-token loss lse_i - z_{i,y_i}
+    (0 when ignored), loss = sum / n ("mean"), sum ("sum") or the per-token
+    vector ("none"); dlogits = (exp(z - lse) - onehot) * grad_scale / n, zero rows
+    for ignored tokens ("none" has no gradient here).
+    Returns dict(loss, lse, nll, n_valid, dZ)."""
+    Z = np.asarray(Z)
+    N, V = Z.shape
+    if reduction not in ("mean", "sum", "none"):
+        raise ValueError(f"unsupported reduction {reduction!r}")
+    valid = check_labels(labels, V, ignore_index)
+    y = np.where(valid, np.asarray(labels, dtype=np.int64), 0)
+    n_valid = int(np.count_nonzero(valid))
+    if reduction == "sum":
+        scale = grad_scale
+    elif normalizer > 0:
+        scale = grad_scale / normalizer
+    else:
+        scale = grad_scale / n_valid if n_valid > 0 else 0.0
+    lse = np.empty(N, dtype=np.float64)
+    nll = np.zeros(N, dtype=np.float64)
+    dZ = np.zeros((N, V), dtype=np.float64) if (want_grad and reduction != "none") else None
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        Zb = Z[r0:r1].astype(np.float64)
+        lse_b = log_sum_exp_rows(Zb)
+        lse[r0:r1] = lse_b
+        k = np.arange(r1 - r0)
+        nll[r0:r1] = np.where(valid[r0:r1], lse_b - Zb[k, y[r0:r1]], 0.0)
+        if dZ is not None:
+            G = np.exp(Zb - lse_b[:, None])
+            G[k, y[r0:r1]] -= 1.0
+            G *= scale
+            G[~valid[r0:r1]] = 0.0
+            dZ[r0:r1] = G
+    total = math.fsum(nll[valid].tolist())
+    if reduction == "none":
+        loss = nll.copy()
+    elif reduction == "sum":
+        loss = total
+    elif normalizer > 0:
+        loss = total / normalizer
+    else:
+        loss = total / n_valid if n_valid > 0 else 0.0
+    return dict(loss=loss, lse=lse, nll=nll, n_valid=n_valid, dZ=dZ)
 
 
 def logits_bytes(N: int, V: int, elem_bytes: int = 4) -> int:

@@ -23,7 +23,8 @@ def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
-                            "flce_check_status", "flce_status_string"])
+                            "flce_ce_workspace_size", "flce_ce_logits", "flce_check_status",
+                            "flce_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -111,6 +112,28 @@ def test_plan_rejections_before_device_query():
     assert flce.lib.flce_get_plan(64, 128, 1000, None, 1, 1, None) == flce.FLCE_ERR_NULL
     assert flce.lib.flce_get_plan(0, 128, 1000, None, 1, 1, ctypes.byref(info)) == flce.FLCE_ERR_SHAPE
     assert flce.lib.flce_get_plan(64, 12, 1000, None, 1, 1, ctypes.byref(info)) == flce.FLCE_ERR_ALIGN
+
+
+def test_ce_logits_host_rejections():
+    f = flce.lib.flce_ce_logits
+    ws = ctypes.c_size_t()
+    assert flce.lib.flce_ce_workspace_size(8, 100, None, ctypes.byref(ws)) == flce.FLCE_OK
+    assert ws.value >= 2 * 8 * 4
+
+    def call(logits=0x1000, dtype=0, ld=128, y=0x2000, N=8, V=100, loss=0x3000, dl=None,
+             dld=0, w=0x4000, opts=None):
+        return f(logits, dtype, ld, y, N, V, ctypes.byref(opts) if opts else None, loss, None,
+                 dl, dld, w, 1 << 20, None, None)
+
+    assert call(logits=None) == flce.FLCE_ERR_NULL
+    assert call(N=0) == flce.FLCE_ERR_SHAPE
+    assert call(ld=99) == flce.FLCE_ERR_SHAPE
+    assert call(ld=102) == flce.FLCE_ERR_ALIGN          # 408-byte rows
+    assert call(dtype=1, ld=100) == flce.FLCE_ERR_ALIGN  # 200-byte rows
+    assert call(dtype=7) == flce.FLCE_ERR_OPTION
+    assert call(dl=0x1000, dld=256) == flce.FLCE_ERR_OPTION  # in place with another stride
+    o = flce.make_options(reduction="none")
+    assert call(dl=0x8000, dld=128, opts=o) == flce.FLCE_ERR_OPTION
 
 
 def test_status_strings():

@@ -1,0 +1,128 @@
+"""GPU parity of the cross-entropy over given logits (flce_ce_logits) against
+the CPU float64 oracle's ce_logits, with the numerics gate of the fused path
+(loss rel 1e-3, lse abs 2e-3, gradient relative Frobenius 5e-3)."""
+import numpy as np
+import pytest
+
+import flce_inputs
+import oracle
+from flce_testlib import rel_fro, tensor_to_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import linear_cross_entropy_flce_gb300 as flce
+
+
+def _logits(N, V, seed, std=1.3, ld=None, bf16=False, p_ignore=0.05):
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, 91])))
+    Z = (g.standard_normal((N, V), dtype=np.float32) * np.float32(std))
+    if bf16:
+        Z = flce_inputs.bf16_bits_to_f32(flce_inputs.f32_to_bf16_bits(Z))
+    y = g.integers(0, V, N).astype(np.int32)
+    k = int(round(p_ignore * N))
+    if k:
+        y[g.permutation(N)[:k]] = -100
+    ld = ld or V
+    dev = torch.device("cuda:0")
+    full = torch.zeros(N, ld, dtype=torch.float32)
+    full[:, :V] = torch.from_numpy(Z)
+    t = full.to(dev)
+    if bf16:
+        t = t.to(torch.bfloat16)
+    return Z.astype(np.float64), y, t[:, :V], torch.from_numpy(y).to(dev)
+
+
+def _check(res, ref, grad=True, per_token=False):
+    if per_token:
+        assert np.max(np.abs(res.loss.double().cpu().numpy() - ref["loss"])) <= 2e-3
+    else:
+        loss = float(res.loss.item())
+        assert abs(loss - ref["loss"]) <= 1e-3 * max(abs(ref["loss"]), 1e-30)
+    assert np.max(np.abs(res.lse.double().cpu().numpy() - ref["lse"])) <= 2e-3
+    if grad:
+        err = rel_fro(tensor_to_f64(res.dlogits), ref["dZ"])
+        assert err <= 5e-3, err
+
+
+@pytest.mark.parametrize("N,V,ld", [(333, 5003, 5004), (1, 3, 4), (64, 4096, 4096), (257, 32000, 32008)])
+def test_fp32_logits_parity(N, V, ld):
+    Z, y, t, lab = _logits(N, V, seed=N + V, ld=ld)
+    res = flce.ce_logits(t, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    _check(res, oracle.ce_logits(Z, y))
+
+
+@pytest.mark.parametrize("N,V", [(200, 32000), (77, 1001)])
+def test_bf16_logits_parity(N, V):
+    ld = (V + 7) // 8 * 8
+    Z, y, t, lab = _logits(N, V, seed=N * 3 + V, bf16=True, ld=ld)
+    res = flce.ce_logits(t, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    _check(res, oracle.ce_logits(Z, y))
+
+
+def test_in_place_equals_out_of_place():
+    for bf16 in (False, True):
+        Z, y, t, lab = _logits(300, 12000, seed=41, bf16=bf16)
+        a = flce.ce_logits(t.clone(), lab)
+        tc = t.clone()
+        b = flce.ce_logits(tc, lab, in_place=True)
+        torch.cuda.synchronize()
+        assert b.dlogits.data_ptr() == tc.data_ptr()
+        assert torch.equal(a.dlogits.view(torch.int16 if bf16 else torch.int32),
+                           b.dlogits.view(torch.int16 if bf16 else torch.int32))
+        assert torch.equal(a.loss, b.loss) and torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("opts", [{"reduction": "sum"}, {"grad_scale": 3.0}, {"normalizer": 500.0}])
+def test_reductions_and_scales(opts):
+    Z, y, t, lab = _logits(150, 2048, seed=42, p_ignore=0.2)
+    res = flce.ce_logits(t, lab, **opts)
+    _check(res, oracle.ce_logits(Z, y, **opts))
+
+
+def test_per_token_losses_forward_only():
+    Z, y, t, lab = _logits(150, 2048, seed=43, p_ignore=0.2)
+    res = flce.ce_logits(t, lab, need_grad=False, reduction="none")
+    _check(res, oracle.ce_logits(Z, y, reduction="none"), grad=False, per_token=True)
+
+
+def test_large_magnitude_logits_are_stable():
+    Z, y, t, lab = _logits(64, 3000, seed=44, std=40.0)
+    res = flce.ce_logits(t, lab)
+    assert torch.isfinite(res.dlogits).all()
+    _check(res, oracle.ce_logits(Z, y))
+
+
+def test_label_edges_and_all_ignored():
+    Z, y, t, lab = _logits(128, 1000, seed=45, p_ignore=0.0)
+    y[:40] = 0
+    y[40:80] = 999
+    lab = torch.from_numpy(y).to(t.device)
+    _check(flce.ce_logits(t, lab), oracle.ce_logits(Z, y))
+    y[:] = -100
+    lab = torch.from_numpy(y).to(t.device)
+    res = flce.ce_logits(t, lab)
+    assert float(res.loss.item()) == 0.0 and torch.count_nonzero(res.dlogits).item() == 0
+    y[5] = 1000
+    lab = torch.from_numpy(y).to(t.device)
+    res = flce.ce_logits(t, lab)
+    assert flce.check_status(res.status) == flce.FLCE_ERR_LABEL_RANGE
+
+
+def test_matches_fused_loss_on_the_same_logits():
+    """The unfused loss over Z = H W^T (computed here in float64 and rounded to
+    fp32) agrees with the fused loss of (H, W) within the numerics gate."""
+    wl = flce_inputs.Workload("ce_vs_flce", 256, 512, 4000, 1.0, 0.05, "uniform", 0.1, seed=46)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    Hd, Wd = flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb)
+    Z = (Hd @ Wd.T).astype(np.float32)
+    dev = torch.device("cuda:0")
+    ce = flce.ce_logits(torch.from_numpy(Z).to(dev), torch.from_numpy(y).to(dev))
+    from flce_testlib import to_device
+    fu = flce.forward(*to_device(Hb, Wb, y))
+    torch.cuda.synchronize()
+    assert abs(float(ce.loss.item()) - float(fu.loss.item())) <= 1e-4 * float(fu.loss.item())
+    assert float((ce.lse - fu.lse).abs().max()) <= 1e-3

@@ -228,3 +228,53 @@ def test_bounded_wait_timeout_sets_status_and_context_stays_usable():
     res = flce.forward_backward(H, W, lab, timeout_ns=1)
     assert flce.check_status(res.status) == flce.FLCE_ERR_TIMEOUT
     _run_and_compare(Hb, Wb, y)
+
+
+def test_forward_per_token_loss_reduction_none():
+    """reduction="none" (forward only): each token's lse_i - z_{i,y_i}, 0 for
+    ignored tokens, against the oracle's per-token NLL; the backward rejects it."""
+    Hb, Wb, y = _inputs(333, 256, 3000, seed=24, p_ignore=0.1)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward(H, W, lab, reduction="none")
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y,
+                      want_grads=False)
+    per = res.loss.double().cpu().numpy()
+    assert per.shape == (333,)
+    assert np.max(np.abs(per - ref["nll"])) <= 2e-3
+    assert np.all(per[y == -100] == 0.0)
+    mean = flce.forward(H, W, lab)
+    assert abs(per[y != -100].mean() - float(mean.loss.item())) <= 1e-5 * float(mean.loss.item())
+    with pytest.raises(flce.FLCEError) as e:
+        flce.forward_backward(H, W, lab, reduction="none")
+    assert e.value.code == flce.FLCE_ERR_OPTION
+
+
+def test_forward_only_matches_oracle_on_llama2_workload():
+    """The evaluation path alone (flce_forward) on the Llama-2-like head."""
+    Hb, Wb, y = flce_inputs.make_inputs(flce_inputs.get("llama2"))
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward(H, W, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f32(Hb), flce_inputs.bf16_bits_to_f32(Wb), y,
+                      want_grads=False)
+    assert abs(float(res.loss.item()) - ref["loss"]) <= 1e-3 * ref["loss"]
+    assert np.max(np.abs(res.lse.double().cpu().numpy() - ref["lse"])) <= 2e-3
+
+
+def test_million_token_vocabulary_full_parity():
+    """V >= 1M (the open question on the lecture page about very large
+    vocabularies): 1,100,000 ids, a ragged final tile, 68 vocabulary chunks in
+    the default plan; every lse, dH and dW element against the oracle."""
+    N, D, V = 300, 128, 1_100_000
+    Hb, Wb, y = _inputs(N, D, V, seed=25, w_std=0.05, p_ignore=0.05)
+    H, W, lab = to_device(Hb, Wb, y)
+    res = flce.forward_backward(H, W, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    plan = flce.get_plan(N, D, V)
+    assert plan["n_chunks"] > 8
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f32(Hb), flce_inputs.bf16_bits_to_f32(Wb), y,
+                      row_block=32)
+    errs = compare(res, ref)
+    print(errs)
+    assert_within(errs)

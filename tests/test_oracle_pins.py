@@ -325,3 +325,61 @@ def test_sample_helpers_are_deterministic_and_cover_edge_ids():
     assert np.sum(y[a] == -100) >= 16
     v = oracle.sample_vocab(y, 1000, 64, seed=0)
     assert 999 in v and len(v) == 64 and np.all(np.diff(v) > 0)
+
+
+# ---- cross-entropy over given logits ----------------------------------------------
+
+def test_ce_logits_zero_logits_closed_form():
+    """Z = 0: lse = log V for every token, loss = log V, dZ = (1/V - onehot)/n."""
+    N, V = 6, 9
+    y = np.array([0, 8, -100, 3, 3, 5])
+    r = oracle.ce_logits(np.zeros((N, V)), y)
+    assert np.all(r["lse"] == math.log(V))
+    assert r["loss"] == pytest.approx(math.log(V), rel=1e-15)
+    n = 5
+    expect = np.full((N, V), 1.0 / V / n)
+    expect[2] = 0.0
+    for i, t in enumerate(y):
+        if t != -100:
+            expect[i, t] -= 1.0 / n
+    np.testing.assert_allclose(r["dZ"], expect, rtol=0, atol=1e-16)
+
+
+def test_ce_logits_two_class_closed_form():
+    """V = 2: loss_i = softplus(z_other - z_target), dz_target = -sigmoid(z_other - z_target)/n."""
+    Z = np.array([[0.3, -1.2], [2.0, 0.5], [-0.7, 0.4]])
+    y = np.array([0, 1, 1])
+    r = oracle.ce_logits(Z, y)
+    d = np.array([Z[0, 1] - Z[0, 0], Z[1, 0] - Z[1, 1], Z[2, 0] - Z[2, 1]])
+    assert r["loss"] == pytest.approx(np.log1p(np.exp(d)).mean(), rel=1e-14)
+    sig = 1 / (1 + np.exp(-d))
+    for i in range(3):
+        assert r["dZ"][i, y[i]] == pytest.approx(-sig[i] / 3, rel=1e-13)
+        assert r["dZ"][i, 1 - y[i]] == pytest.approx(sig[i] / 3, rel=1e-13)
+
+
+def test_ce_logits_central_differences():
+    g = np.random.default_rng(30)
+    Z = g.standard_normal((4, 7)) * 3
+    y = np.array([1, -100, 6, 0])
+    r = oracle.ce_logits(Z, y, reduction="sum", grad_scale=0.5)
+    h = 1e-6
+    for i in range(4):
+        for v in range(7):
+            Zp, Zm = Z.copy(), Z.copy()
+            Zp[i, v] += h
+            Zm[i, v] -= h
+            num = 0.5 * (oracle.ce_logits(Zp, y, reduction="sum", want_grad=False)["loss"] -
+                         oracle.ce_logits(Zm, y, reduction="sum", want_grad=False)["loss"]) / (2 * h)
+            assert r["dZ"][i, v] == pytest.approx(num, rel=1e-6, abs=1e-9)
+
+
+def test_ce_logits_none_reduction_and_large_logits():
+    """Per-token losses; logits near 800 where exp overflows a double."""
+    Z = np.array([[800.0, 799.0, 790.0], [-750.0, -760.0, -751.0]])
+    y = np.array([1, -100])
+    r = oracle.ce_logits(Z, y, reduction="none")
+    mpmath.mp.dps = 50
+    exact = mpmath.log(mpmath.fsum(mpmath.exp(mpmath.mpf(z)) for z in Z[0])) - 799
+    assert r["loss"][0] == pytest.approx(float(exact), rel=1e-14)
+    assert r["loss"][1] == 0.0 and r["dZ"] is None
