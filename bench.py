@@ -286,6 +286,83 @@ def run_forward_only(args, wl, world, rank, local):
     return 0
 
 
+def run_ce_logits(args, wl, world, rank, local):
+    """Cross-entropy over given logits [N, V]: one step = loss, lse and the
+    gradient written to a second buffer (flce_ce_logits). HBM-bound: the
+    algorithmic bytes are one read and one write of the logits."""
+    import torch
+    import linear_cross_entropy_flce_gb300 as flce
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rep = Replicas(world, rank)
+    peaks = load_peaks()
+    N, V = wl.N, wl.V
+    sigma = wl.h_scale * wl.w_std * (wl.D ** 0.5)   # logit std of the fused workload
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([wl.seed, 90])))
+    dt = torch.float32 if args.ce_logits == "float32" else torch.bfloat16
+    Z = torch.empty(N, V, dtype=dt, device=dev)
+    rows = 1024
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        blk = g.standard_normal((r1 - r0, V), dtype=np.float32) * np.float32(sigma)
+        Z[r0:r1].copy_(torch.from_numpy(blk))
+    lab = torch.from_numpy(flce_inputs.make_labels(wl)).to(dev)
+    elt = Z.element_size()
+    out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+           "lse": torch.empty(N, dtype=torch.float32, device=dev),
+           "dlogits": torch.empty_like(Z)}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(**kw):
+        flce.ce_logits(Z, lab, out=out, status=status, stream=stream.cuda_stream, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    if flce.check_status(status, stream.cuda_stream) != flce.FLCE_OK:
+        raise RuntimeError("device status error")
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        rep.barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        rep.barrier()
+    ms = rep.max(ev0.elapsed_time(ev1) / args.steps)
+    # per-kernel: count, rows, reduce
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    rows_ms = 0.0
+    for _ in range(args.steps):
+        step(trace_events=evs)
+        torch.cuda.synchronize(dev)
+        rows_ms += evs[1].elapsed_time(evs[2]) / args.steps
+    algo = 2.0 * N * V * elt + N * 12
+    achieved = algo / (rows_ms / 1e3) / 1e9
+    line = {"metric": "cross-entropy over given logits (loss + gradient) tokens/s",
+            "value": N * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if elt == 4 else "bf16", "data": "synthetic (seeded normal logits)",
+            "config": {"workload": f"logits [{N}, {V}] {args.ce_logits}, labels of {wl.name}",
+                       "N": N, "V": V, "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "unit": "GB/s", "kernel": "ce_rows_kernel",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "frac": achieved / peaks["hbm_gbs"], "ms_per_launch": rows_ms,
+                         "algorithmic_bytes_per_launch": algo, "traffic": None},
+            "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    rep.close()
+    return 0
+
+
 def config_block(wl, world) -> dict:
     return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens, D={wl.D}, V={wl.V}, "
                         f"labels {wl.labels}, {int(round(wl.p_ignore * 100))}% ignore_index=-100",
@@ -311,6 +388,8 @@ def main(argv=None) -> int:
     ap.add_argument("--n-block", type=int, default=0, help="plan override: tokens per block")
     ap.add_argument("--forward-only", action="store_true",
                     help="time flce_forward (loss and lse, the evaluation path) instead")
+    ap.add_argument("--ce-logits", choices=["float32", "bfloat16"], default=None,
+                    help="time the cross-entropy over given [N, V] logits (loss + gradient) instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
@@ -325,6 +404,8 @@ def main(argv=None) -> int:
         return run_reference(args, wl, world, rank)
     if args.forward_only:
         return run_forward_only(args, wl, world, rank, local)
+    if args.ce_logits:
+        return run_ce_logits(args, wl, world, rank, local)
 
     import torch
     import linear_cross_entropy_flce_gb300 as flce
@@ -336,9 +417,11 @@ def main(argv=None) -> int:
 
     # Inputs: seeded host draw, pinned host copy (e2e) and device copy (resident).
     Hb, Wb, y = flce_inputs.make_inputs(wl)
-    H_host = torch.from_numpy(Hb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    W_host = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    y_host = torch.from_numpy(y).pin_memory()
+    H_host = torch.from_numpy(Hb.view(np.int16)).view(torch.bfloat16)
+    W_host = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16)
+    y_host = torch.from_numpy(y)
+    if not args.no_e2e:   # page-locked host buffers for the end-to-end leg
+        H_host, W_host, y_host = H_host.pin_memory(), W_host.pin_memory(), y_host.pin_memory()
     H = H_host.to(dev)
     W = W_host.to(dev)
     lab = y_host.to(dev)

@@ -288,8 +288,8 @@ def ce_logits(logits, labels, *, need_grad: bool = True, in_place: bool = False,
     grad = None
     if need_grad:
         grad = logits if in_place else out.get("dlogits")
-        if grad is None:
-            grad = torch.empty_like(logits)
+        if grad is None:   # same (padded) row stride as the logits
+            grad = torch.empty_strided((N, V), (ld, 1), dtype=logits.dtype, device=dev)
     size = ctypes.c_size_t(0)
     rc = lib.flce_ce_workspace_size(N, V, ctypes.byref(opts), ctypes.byref(size))
     if rc != FLCE_OK:

@@ -627,9 +627,8 @@ int flce_ce_logits(const void* logits, int32_t dtype, int64_t ld, const int32_t*
                              o.normalizer, scal, status, st) != cudaSuccess ||
        !trace()))
     return FLCE_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(N, static_cast<int64_t>(sms) * 4));
   if (flce::launch_ce_rows(dtype == FLCE_DTYPE_BF16 ? 1 : 0, logits, ld * elt, labels, Ni, Vi,
-                           o.ignore_index, scal, lse ? lse : lse_ws, nll, dlogits, dld * elt, grid,
+                           o.ignore_index, scal, lse ? lse : lse_ws, nll, dlogits, dld * elt, sms,
                            st) != cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;

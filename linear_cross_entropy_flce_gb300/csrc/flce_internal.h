@@ -41,7 +41,7 @@ cudaError_t launch_ce_count(const int32_t* labels, int N, int V, int ignore_inde
                             cudaStream_t stream);
 cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int32_t* labels,
                            int N, int V, int ignore_index, const float* scale, float* lse,
-                           float* nll, void* g, int64_t gld_bytes, int grid,
+                           float* nll, void* g, int64_t gld_bytes, int sms,
                            cudaStream_t stream);
 
 }  // namespace flce
