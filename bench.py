@@ -390,6 +390,9 @@ def main(argv=None) -> int:
                     help="time flce_forward (loss and lse, the evaluation path) instead")
     ap.add_argument("--ce-logits", choices=["float32", "bfloat16"], default=None,
                     help="time the cross-entropy over given [N, V] logits (loss + gradient) instead")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 operand variant: E4M3 H and W (per-tensor scales) for the two "
+                         "logits products, bf16 H and W for the gradient products")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
@@ -406,6 +409,9 @@ def main(argv=None) -> int:
         return run_forward_only(args, wl, world, rank, local)
     if args.ce_logits:
         return run_ce_logits(args, wl, world, rank, local)
+    if args.fp8:
+        args.no_e2e = True
+        args.no_cpu_baseline = True
 
     import torch
     import linear_cross_entropy_flce_gb300 as flce
@@ -426,6 +432,11 @@ def main(argv=None) -> int:
     W = W_host.to(dev)
     lab = y_host.to(dev)
     N, D, V = wl.N, wl.D, wl.V
+    fp8 = None
+    if args.fp8:   # input preparation, outside every timed region
+        H8, sh = flce_inputs.to_fp8_per_tensor(Hb)
+        W8, sw = flce_inputs.to_fp8_per_tensor(Wb)
+        fp8 = (torch.from_numpy(H8).to(dev), float(sh), torch.from_numpy(W8).to(dev), float(sw))
 
     plan_kw = {"v_chunk": args.v_chunk, "n_block": args.n_block}
     opts = flce.make_options(**plan_kw)
@@ -445,9 +456,17 @@ def main(argv=None) -> int:
     base = torch.cuda.memory_allocated(dev)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
+    def call(**kw):
+        if fp8 is not None:
+            flce.forward_backward_fp8(fp8[0], fp8[1], fp8[2], fp8[3], lab, H, W, out=out,
+                                      workspace=ws, status=status, stream=stream.cuda_stream,
+                                      **plan_kw, **kw)
+        else:
+            flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
+                                  stream=stream.cuda_stream, **plan_kw, **kw)
+
     def step():
-        flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
-                              stream=stream.cuda_stream, **plan_kw)
+        call()
 
     for _ in range(args.warmup):
         step()
@@ -486,8 +505,7 @@ def main(argv=None) -> int:
     per_kind = {k: 0.0 for k in kinds}
     n_kind = {k: 0 for k in kinds}
     for _ in range(args.steps):
-        flce.forward_backward(H, W, lab, out=out, workspace=ws, status=status,
-                              stream=stream.cuda_stream, trace_events=evs, **plan_kw)
+        call(trace_events=evs)
         torch.cuda.synchronize(dev)
         for k in range(n_launch):
             per_kind[kinds[k]] += evs[k].elapsed_time(evs[k + 1])
@@ -587,10 +605,19 @@ def main(argv=None) -> int:
                "sample": f"first {r['tokens']} tokens of the {wl.name} workload, full V={V} "
                          f"and D={D}, float64 fwd+bwd (loss, lse, dH, dW)"}
 
+    if fp8 is not None:
+        # the two logits products run on E4M3 operands: their peak is the measured
+        # bf16 peak x the nominal FP8/bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+        fp8_peak = 2.0 * peak
+        for k in ("lse_gemm", "grad_gemm"):
+            roofline["kernels"][k]["peak_fp8"] = fp8_peak
+            roofline["kernels"][k]["frac_of_fp8_peak"] = roofline["kernels"][k]["tflops"] / fp8_peak
+        roofline["note_fp8"] = ("lse_gemm and grad_gemm use E4M3 operands (kind::f8f6f4); "
+                                "peak_fp8 = 2 x the measured bf16 peak (nominal ratio)")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; no dataset or weights)",
+        "vs_baseline": None, "dtype": "e4m3 logits products + bf16 gradient products" if fp8 else "bf16", "data": "synthetic (seeded; no dataset or weights)",
         "config": config_block(wl, world),
         "tflops": tflops, "frac_bf16_peak": tflops / peak,
         "peak_extra_hbm_bytes": int(peak_delta),

@@ -164,6 +164,30 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
                  size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * FP8 operand variant (the lecture notes' open question on FP8 matrix units):
+ * the logits are computed from E4M3 operands with per-tensor scales,
+ *     z_iv = scale_h * scale_w * (H8_i . W8_v)     (E4M3 x E4M3, fp32 accumulate),
+ * with tcgen05 kind::f8f6f4 for both logits products (the forward LSE pass and
+ * the recompute of G); loss, lse and G follow from z exactly as in the bf16 path.
+ * The gradient products take the bf16 tensors the FP8 operands were made from:
+ * dH = G W and dW = G^T H (straight through the quantisation).
+ *   H8 [N, D], W8 [V, D]  E4M3 bytes, row-major, 16-byte aligned, D % 16 == 0
+ *   scale_h, scale_w      positive fp32 scales (dequantised value = scale * e4m3)
+ *   H, W                  bf16 [N, D], [V, D] (flce_forward_backward_fp8 only)
+ * Other arguments, outputs, workspace (flce_workspace_size) and errors as in
+ * flce_forward / flce_forward_backward.
+ */
+int flce_forward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+                     const int32_t* labels, int64_t N, int64_t D, int64_t V,
+                     const flce_options* opt, float* loss, float* lse, void* workspace,
+                     size_t ws_bytes, int32_t* status, void* stream);
+int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+                              const uint16_t* H, const uint16_t* W, const int32_t* labels,
+                              int64_t N, int64_t D, int64_t V, const flce_options* opt,
+                              float* loss, float* lse, uint16_t* dH, void* dW, void* workspace,
+                              size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * flce_forward, for callers that cannot allocate device memory at call time and
  * so cannot pass a workspace: for example a plugin whose host application owns
  * all device memory and gives it no allocator, or a server that reserved its

@@ -89,6 +89,14 @@ lib.flce_ce_workspace_size.restype = ctypes.c_int
 lib.flce_ce_logits.argtypes = [_vp, ctypes.c_int32, _i64, _vp, _i64, _i64, ctypes.POINTER(Options),
                                _vp, _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_ce_logits.restype = ctypes.c_int
+_f32 = ctypes.c_float
+lib.flce_forward_fp8.argtypes = [_vp, _f32, _vp, _f32, _vp, _i64, _i64, _i64,
+                                 ctypes.POINTER(Options), _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+lib.flce_forward_fp8.restype = ctypes.c_int
+lib.flce_forward_backward_fp8.argtypes = [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i64,
+                                          ctypes.POINTER(Options), _vp, _vp, _vp, _vp, _vp,
+                                          ctypes.c_size_t, _vp, _vp]
+lib.flce_forward_backward_fp8.restype = ctypes.c_int
 lib.flce_check_status.argtypes = [_vp, _vp]
 lib.flce_check_status.restype = ctypes.c_int
 lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -308,6 +316,64 @@ def ce_logits(logits, labels, *, need_grad: bool = True, in_place: bool = False,
     r = Result(loss, lse, None, None, status)
     r.dlogits = grad
     return r
+
+
+def forward_backward_fp8(H8, scale_h: float, W8, scale_w: float, labels, H=None, W=None, *,
+                         need_dh: bool = True, need_dw: bool = True, out: Optional[dict] = None,
+                         workspace=None, status=None, stream=None, **options) -> Result:
+    """FP8 operand variant (flce_forward_backward_fp8, or flce_forward_fp8 when no
+    gradient is requested): E4M3 H8 [N, D] and W8 [V, D] (torch.uint8) with
+    per-tensor scales define the logits; the gradient products use bf16 H, W."""
+    import torch
+    grads = need_dh or need_dw
+    if not (H8.is_cuda and W8.is_cuda and labels.is_cuda):
+        raise ValueError("H8, W8 and labels must be CUDA tensors")
+    if H8.dtype != torch.uint8 or W8.dtype != torch.uint8 or labels.dtype != torch.int32:
+        raise TypeError("H8, W8 uint8 (E4M3 bytes), labels int32")
+    if not (H8.is_contiguous() and W8.is_contiguous() and labels.is_contiguous()):
+        raise ValueError("H8, W8 and labels must be contiguous")
+    N, D = H8.shape
+    V = W8.shape[0]
+    if grads:
+        if H is None or W is None:
+            raise ValueError("the gradient products need the bf16 H and W")
+        _check_inputs(H, W, labels)
+    opts = make_options(**options)
+    dev = H8.device
+    out = dict(out or {})
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(N if options.get("reduction") == "none" else 1, dtype=torch.float32,
+                           device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = out.get("dH")
+    if dH is None and need_dh:
+        dH = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = out.get("dW")
+    if dW is None and need_dw:
+        dt = torch.float32 if options.get("dw_dtype", "float32") == "float32" else torch.bfloat16
+        dW = torch.empty(V, D, dtype=dt, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    wsb = workspace.numel() * workspace.element_size()
+    if grads:
+        rc = lib.flce_forward_backward_fp8(
+            _ptr(H8), float(scale_h), _ptr(W8), float(scale_w), _ptr(H), _ptr(W), _ptr(labels),
+            N, D, V, ctypes.byref(opts), _ptr(loss), _ptr(lse), _ptr(dH) if need_dh else None,
+            _ptr(dW) if need_dw else None, _ptr(workspace), wsb, _ptr(status), stream)
+    else:
+        rc = lib.flce_forward_fp8(_ptr(H8), float(scale_h), _ptr(W8), float(scale_w),
+                                  _ptr(labels), N, D, V, ctypes.byref(opts), _ptr(loss),
+                                  _ptr(lse), _ptr(workspace), wsb, _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_backward_fp8" if grads else "flce_forward_fp8")
+    return Result(loss, lse, dH if need_dh else None, dW if need_dw else None, status)
 
 
 def check_status(status, stream=None) -> int:

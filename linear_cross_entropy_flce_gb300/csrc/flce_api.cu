@@ -250,19 +250,55 @@ int check_shape(int64_t N, int64_t D, int64_t V) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
-        int64_t V, const flce_options* opt_in, float* loss, float* lse_out, uint16_t* dH, void* dW,
-        bool backward, void* workspace, size_t ws_bytes, int32_t* status, void* stream_v) {
+// Fp8 carries the E4M3 operands of the FP8 variant (null for the bf16 path):
+// they feed the two logits products; H and W (bf16) feed the gradient products.
+struct Fp8Operands {
+  const uint8_t* H8 = nullptr;
+  const uint8_t* W8 = nullptr;
+  float scale_h = 1.f, scale_w = 1.f;
+};
+
+// uint8 matrix [outer][inner] read in boxes of box_inner x box_outer bytes with
+// 128-byte swizzle; out-of-range elements read as zero.
+bool encode_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32_t* labels,
+        int64_t N, int64_t D, int64_t V, const flce_options* opt_in, float* loss, float* lse_out,
+        uint16_t* dH, void* dW, bool backward, void* workspace, size_t ws_bytes, int32_t* status,
+        void* stream_v) {
   flce_options o;
   flce_default_options(&o);
   if (opt_in != nullptr) o = *opt_in;
-  if (H == nullptr || W == nullptr || labels == nullptr || loss == nullptr || workspace == nullptr)
-    return FLCE_ERR_NULL;
+  const bool fp8 = f8.H8 != nullptr || f8.W8 != nullptr;
+  if (!backward) {
+    dH = nullptr;
+    dW = nullptr;
+  }
+  const bool need_bf16 = !fp8 || dH != nullptr || dW != nullptr;
+  if (labels == nullptr || loss == nullptr || workspace == nullptr) return FLCE_ERR_NULL;
+  if (fp8 && (f8.H8 == nullptr || f8.W8 == nullptr)) return FLCE_ERR_NULL;
+  if (need_bf16 && (H == nullptr || W == nullptr)) return FLCE_ERR_NULL;
   int rc = check_shape(N, D, V);
   if (rc != FLCE_OK) return rc;
   rc = check_options(o);
   if (rc != FLCE_OK) return rc;
-  if (!aligned16(H) || !aligned16(W) || !aligned16(labels) || !aligned16(workspace) ||
+  if (fp8 && (D % 16 != 0 || !aligned16(f8.H8) || !aligned16(f8.W8))) return FLCE_ERR_ALIGN;
+  if (fp8 && !(f8.scale_h > 0.f && f8.scale_w > 0.f && f8.scale_h * f8.scale_w < 3.0e38f))
+    return FLCE_ERR_OPTION;
+  if ((H && !aligned16(H)) || (W && !aligned16(W)) || !aligned16(labels) ||
+      !aligned16(workspace) ||
       (lse_out && !aligned16(lse_out)) || (dH && !aligned16(dH)) || (dW && !aligned16(dW)) ||
       (reinterpret_cast<uintptr_t>(loss) & 3u) || (reinterpret_cast<uintptr_t>(status) & 3u))
     return FLCE_ERR_ALIGN;
@@ -273,10 +309,7 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   rc = make_plan(N, D, V, o, sms, &P);
   if (rc != FLCE_OK) return rc;
   if (ws_bytes < P.total) return FLCE_ERR_WORKSPACE;
-  if (!backward) {
-    dH = nullptr;
-    dW = nullptr;
-  } else if (o.reduction == FLCE_REDUCTION_NONE) {
+  if (backward && o.reduction == FLCE_REDUCTION_NONE) {
     return FLCE_ERR_OPTION;  // a per-token loss needs a per-token upstream gradient
   }
   const bool per_token = o.reduction == FLCE_REDUCTION_NONE;
@@ -311,10 +344,20 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
 
   const int cta = P.cta;
   const int pairs = std::max(1, sms / cta);
+  // Operands of the two logits products: bf16 H, W, or E4M3 H8, W8 (128 bytes =
+  // 128 elements per stage row).
   CUtensorMap mH_k, mW_k;
-  if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) ||
-      !encode_bf16(&mW_k, W, D, V, D, BK, static_cast<uint32_t>(BN / cta)))
+  if (fp8) {
+    if (!encode_u8(&mH_k, f8.H8, D, N, D, 2 * BK, BM) ||
+        !encode_u8(&mW_k, f8.W8, D, V, D, 2 * BK, static_cast<uint32_t>(BN / cta)))
+      return FLCE_ERR_CUDA;
+  } else if (!encode_bf16(&mH_k, H, D, N, D, BK, BM) ||
+             !encode_bf16(&mW_k, W, D, V, D, BK, static_cast<uint32_t>(BN / cta))) {
     return FLCE_ERR_CUDA;
+  }
+  const int k_blocks_z = static_cast<int>(ceil_div(D, fp8 ? 2 * BK : BK));
+  const uint32_t idesc_z = fp8 ? make_idesc_e4m3_f32(P.tile_m, BN) : make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
+  const float acc_scale = fp8 ? f8.scale_h * f8.scale_w : 1.f;
 
   // ---- 1. forward LSE GEMM ----
   GemmParams g{};
@@ -322,12 +365,13 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   g.b_mn_major = 0;
   g.m_blocks = P.m_blocks;
   g.n_blocks = P.v_tiles;
-  g.k_blocks = static_cast<int>(ceil_div(D, BK));
+  g.k_blocks = k_blocks_z;
+  g.acc_scale = acc_scale;
   g.splits = P.splits;
   g.part_stride = P.part_stride;
   g.num_units = P.splits * P.m_blocks;
   g.group_m = std::min(P.m_blocks, 16);
-  g.idesc = make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
+  g.idesc = idesc_z;
   g.timeout_ns = tmo;
   g.status = status;
   g.m_valid = static_cast<int>(N);
@@ -338,7 +382,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
   g.ignore_index = o.ignore_index;
   g.part = part;
   g.zt = zt;
-  if (launch_gemm_lse(cta, mH_k, mW_k, g, cta * std::min(g.num_units, pairs), st) != cudaSuccess ||
+  if (launch_gemm_lse(cta, mH_k, mW_k, g, cta * std::min(g.num_units, pairs), st, fp8 ? 1 : 0) !=
+          cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;
 
@@ -386,10 +431,11 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       q.b_mn0 = static_cast<int>(c0);
       q.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
       q.n_blocks = static_cast<int>(ceil_div(c_len, BN));
-      q.k_blocks = static_cast<int>(ceil_div(D, BK));
+      q.k_blocks = k_blocks_z;
+      q.acc_scale = acc_scale;
       q.num_units = q.m_blocks * q.n_blocks;
       q.group_m = std::min(q.m_blocks, 16);
-      q.idesc = make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
+      q.idesc = idesc_z;
       q.timeout_ns = tmo;
       q.status = status;
       q.m_valid = nb_len;
@@ -402,7 +448,8 @@ int run(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, 
       q.scale = scal;
       q.g_out = G;
       q.g_ld = P.v_chunk;
-      if (launch_gemm_grad(cta, mH_k, mW_k, q, cta * std::min(q.num_units, pairs), st) !=
+      if (launch_gemm_grad(cta, mH_k, mW_k, q, cta * std::min(q.num_units, pairs), st,
+                           fp8 ? 1 : 0) !=
               cudaSuccess ||
           !trace())
         return FLCE_ERR_CUDA;
@@ -645,15 +692,42 @@ int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* l
                           int64_t D, int64_t V, const flce_options* opt, float* loss, float* lse,
                           uint16_t* dH, void* dW, void* workspace, size_t ws_bytes,
                           int32_t* status, void* stream) {
-  return flce::run(H, W, labels, N, D, V, opt, loss, lse, dH, dW, true, workspace, ws_bytes,
-                   status, stream);
+  return flce::run(H, W, flce::Fp8Operands{}, labels, N, D, V, opt, loss, lse, dH, dW, true,
+                   workspace, ws_bytes, status, stream);
 }
 
 int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
                  int64_t V, const flce_options* opt, float* loss, float* lse, void* workspace,
                  size_t ws_bytes, int32_t* status, void* stream) {
-  return flce::run(H, W, labels, N, D, V, opt, loss, lse, nullptr, nullptr, false, workspace,
-                   ws_bytes, status, stream);
+  return flce::run(H, W, flce::Fp8Operands{}, labels, N, D, V, opt, loss, lse, nullptr, nullptr,
+                   false, workspace, ws_bytes, status, stream);
+}
+
+int flce_forward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+                     const int32_t* labels, int64_t N, int64_t D, int64_t V,
+                     const flce_options* opt, float* loss, float* lse, void* workspace,
+                     size_t ws_bytes, int32_t* status, void* stream) {
+  flce::Fp8Operands f8;
+  f8.H8 = H8;
+  f8.W8 = W8;
+  f8.scale_h = scale_h;
+  f8.scale_w = scale_w;
+  return flce::run(nullptr, nullptr, f8, labels, N, D, V, opt, loss, lse, nullptr, nullptr, false,
+                   workspace, ws_bytes, status, stream);
+}
+
+int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+                              const uint16_t* H, const uint16_t* W, const int32_t* labels,
+                              int64_t N, int64_t D, int64_t V, const flce_options* opt,
+                              float* loss, float* lse, uint16_t* dH, void* dW, void* workspace,
+                              size_t ws_bytes, int32_t* status, void* stream) {
+  flce::Fp8Operands f8;
+  f8.H8 = H8;
+  f8.W8 = W8;
+  f8.scale_h = scale_h;
+  f8.scale_w = scale_w;
+  return flce::run(H, W, f8, labels, N, D, V, opt, loss, lse, dH, dW, true, workspace, ws_bytes,
+                   status, stream);
 }
 
 int flce_check_status(const int32_t* status, void* stream) {

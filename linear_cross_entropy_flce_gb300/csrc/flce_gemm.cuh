@@ -171,7 +171,10 @@ __device__ __forceinline__ void f32_chunk(const float (&v)[32], const GemmParams
 
 // ---- the kernel --------------------------------------------------------------------
 
-template <int kEpi, int kCta>
+// kFp8 = 1: A and B are E4M3 bytes (K-major only), 128 of them per 128-byte
+// stage row, multiplied with tcgen05 kind::f8f6f4; the epilogue scales z by
+// p.acc_scale. The shared-memory image of a stage is the same as for bf16.
+template <int kEpi, int kCta, int kFp8 = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t fb = full_bar(stage);
             mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-            const int kx = kb * BK;
+            const int kx = kb * (kFp8 ? 2 * BK : BK);  // elements per 128-byte row
 #pragma unroll
             for (int r = 0; r < kCta; ++r) {
               const uint32_t sa_local = stage0 + stage * Cfg::kStageBytes;
@@ -351,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
               const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
                                        : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
-              umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
+              if constexpr (kFp8) umma_f8_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
+              else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
             }
             issued_any = true;
             umma_commit_cg<kCta>(empty_bar(stage));
@@ -444,6 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= p.acc_scale;
+          }
           const int col = n_blk * BN + c * 32;  // product column
           if constexpr (kEpi == EPI_LSE) {
             lse_chunk(v, col, p.n_valid, y - (p.col_base + col), st);

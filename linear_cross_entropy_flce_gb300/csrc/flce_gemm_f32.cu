@@ -9,7 +9,7 @@ namespace {
 template <int kCta>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                    cudaStream_t stream) {
-  auto kern = flce_gemm_kernel<EPI_F32, kCta>;
+  auto kern = flce_gemm_kernel<EPI_F32, kCta, 0>;
   constexpr size_t smem = TileCfg<kCta>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

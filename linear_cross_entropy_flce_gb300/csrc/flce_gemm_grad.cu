@@ -6,10 +6,10 @@ namespace flce {
 
 namespace {
 
-template <int kCta>
+template <int kCta, int kFp8>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
                    cudaStream_t stream) {
-  auto kern = flce_gemm_kernel<EPI_GRAD, kCta>;
+  auto kern = flce_gemm_kernel<EPI_GRAD, kCta, kFp8>;
   constexpr size_t smem = TileCfg<kCta>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -32,8 +32,9 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
 }  // namespace
 
 cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                           const GemmParams& p, int grid, cudaStream_t stream) {
-  return cta_group == 2 ? launch<2>(a, b, p, grid, stream) : launch<1>(a, b, p, grid, stream);
+                           const GemmParams& p, int grid, cudaStream_t stream, int fp8) {
+  if (fp8) return cta_group == 2 ? launch<2, 1>(a, b, p, grid, stream) : launch<1, 1>(a, b, p, grid, stream);
+  return cta_group == 2 ? launch<2, 0>(a, b, p, grid, stream) : launch<1, 0>(a, b, p, grid, stream);
 }
 
 }  // namespace flce

@@ -50,6 +50,12 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int M, int N, int a_m
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0) and an
+// fp32 accumulator: the same field positions as kind::f16.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 struct GemmParams {
   // operand geometry: coordinates of tile (m, n, k) in the tensor maps are
   //   K-major  operand: x = k*BK + k0,         y = mn*BLOCK + mn0
@@ -67,6 +73,7 @@ struct GemmParams {
                 // walk the vocabulary ranges together)
   int a_hint, b_hint;  // L2 policy of the A / B loads: 0 none, 1 evict_first, 2 evict_last
   uint32_t idesc;
+  float acc_scale;   // FP8 operands: z = acc_scale * accumulator (scale_h * scale_w)
   int64_t timeout_ns;
   int32_t* status;
   int m_valid;  // rows of the product that exist

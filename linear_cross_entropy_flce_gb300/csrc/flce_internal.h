@@ -12,10 +12,11 @@
 namespace flce {
 
 // cta_group 1: grid CTAs of one; cta_group 2: grid/2 clusters of two CTAs.
+// fp8 = 1: E4M3 operands (kind::f8f6f4) scaled by p.acc_scale in the epilogue.
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                            const GemmParams& p, int grid, cudaStream_t stream);
+                            const GemmParams& p, int grid, cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                             const GemmParams& p, int grid, cudaStream_t stream);
+                             const GemmParams& p, int grid, cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t stream);
 

@@ -82,7 +82,8 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
          ignore_index: int = IGNORE_INDEX, reduction: str = "mean",
          grad_scale: float = 1.0, normalizer: float = 0.0,
          dh_rows: Optional[Sequence[int]] = None, dw_rows: Optional[Sequence[int]] = None,
-         want_grads: bool = True, row_block: int = 512, vocab_block: int = 4096) -> dict:
+         want_grads: bool = True, row_block: int = 512, vocab_block: int = 4096,
+         Hg: Optional[np.ndarray] = None, Wg: Optional[np.ndarray] = None) -> dict:
     """Loss, per-token LSE and gradients of fused linear cross-entropy, float64.
 
     H: [N, D], W: [V, D] (any real dtype; values are taken exactly in float64),
@@ -90,15 +91,22 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
     `normalizer` when it is > 0), "sum" does not divide.
 
     dh_rows / dw_rows select which rows of dH (token ids) and dW (vocabulary ids)
-    are computed; None means all. lse is always computed for every token because
+    are computed; None means all.
+    Hg / Wg (default H / W) are the operands of the two gradient products,
+    dH = G Wg and dW = G^T Hg. The FP8 variant passes the dequantised FP8
+    operands as H, W (they define the logits) and their bf16 originals as Hg, Wg. lse is always computed for every token because
     the loss and every dW row need all of them.
     Returns dict(loss, lse[N], nll[N] (0 on ignored tokens), n_valid, dH, dW,
     dh_rows, dw_rows).
     """
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
+    Hg = H if Hg is None else np.asarray(Hg, dtype=np.float64)
+    Wg = W if Wg is None else np.asarray(Wg, dtype=np.float64)
     N, D = H.shape
     V, D2 = W.shape
+    if Hg.shape != H.shape or Wg.shape != W.shape:
+        raise ValueError("gradient operands must match H and W in shape")
     if D != D2:
         raise ValueError("H and W disagree on the hidden size")
     if reduction not in ("mean", "sum"):
@@ -141,7 +149,7 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
                 G[np.arange(len(sel)), y[sel]] -= 1.0
                 G *= scale
                 G[~valid[sel]] = 0.0
-                out = G @ W
+                out = G @ Wg
                 for k, r in enumerate(sel):
                     dH[dh_pos[int(r)]] = out[k]
 
@@ -159,6 +167,7 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
         # dW_v = sum_i g_iv h_i for every v in the block.
         dW = np.zeros((len(dw_sel), D), dtype=np.float64)
         Hv = H[valid]
+        Hgv = Hg[valid]
         yv = y[valid]
         lsev = lse[valid]
         for c0 in range(0, len(dw_sel), vocab_block):
@@ -167,7 +176,7 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
             Gc = np.exp(Zc - lsev[:, None])
             Gc -= (yv[:, None] == vids[None, :])
             Gc *= scale
-            dW[c0:c0 + len(vids)] = Gc.T @ Hv
+            dW[c0:c0 + len(vids)] = Gc.T @ Hgv
 
     return dict(loss=loss, lse=lse, nll=nll, n_valid=n_valid, dH=dH, dW=dW,
                 dh_rows=dh_sel, dw_rows=dw_sel)

@@ -23,7 +23,8 @@ def test_header_declares_the_abi():
     names = declared_functions()
     assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
-                            "flce_ce_workspace_size", "flce_ce_logits", "flce_check_status",
+                            "flce_ce_workspace_size", "flce_ce_logits", "flce_forward_fp8",
+                            "flce_forward_backward_fp8", "flce_check_status",
                             "flce_status_string"])
 
 
@@ -134,6 +135,28 @@ def test_ce_logits_host_rejections():
     assert call(dl=0x1000, dld=256) == flce.FLCE_ERR_OPTION  # in place with another stride
     o = flce.make_options(reduction="none")
     assert call(dl=0x8000, dld=128, opts=o) == flce.FLCE_ERR_OPTION
+
+
+def test_fp8_host_rejections():
+    f = flce.lib.flce_forward_fp8
+    ok = dict(H8=0x1000, sh=1.0, W8=0x2000, sw=1.0, y=0x3000, N=64, D=128, V=1000, loss=0x4000,
+              ws=0x5000)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["H8"], a["sh"], a["W8"], a["sw"], a["y"], a["N"], a["D"], a["V"], None,
+                 a["loss"], None, a["ws"], 1 << 30, None, None)
+
+    assert call(H8=None) == flce.FLCE_ERR_NULL
+    assert call(W8=None) == flce.FLCE_ERR_NULL
+    assert call(D=136) == flce.FLCE_ERR_ALIGN      # D % 16 != 0 for E4M3 rows
+    assert call(H8=0x1004) == flce.FLCE_ERR_ALIGN
+    assert call(sh=0.0) == flce.FLCE_ERR_OPTION
+    assert call(sw=-1.0) == flce.FLCE_ERR_OPTION
+    g = flce.lib.flce_forward_backward_fp8
+    # the gradient products need the bf16 operands
+    assert g(0x1000, 1.0, 0x2000, 1.0, None, None, 0x3000, 64, 128, 1000, None, 0x4000, None,
+             0x6000, 0x7000, 0x5000, 1 << 30, None, None) == flce.FLCE_ERR_NULL
 
 
 def test_status_strings():

@@ -383,3 +383,20 @@ def test_ce_logits_none_reduction_and_large_logits():
     exact = mpmath.log(mpmath.fsum(mpmath.exp(mpmath.mpf(z)) for z in Z[0])) - 799
     assert r["loss"][0] == pytest.approx(float(exact), rel=1e-14)
     assert r["loss"][1] == 0.0 and r["dZ"] is None
+
+
+def test_gradient_operands_enter_only_the_two_products():
+    """With Hg, Wg given, the loss and lse still come from H, W, and the
+    gradients are the same G times the substituted operands."""
+    H, W, y = _rand(31, 6, 5, 9)
+    g = np.random.default_rng(32)
+    Hg = H + g.standard_normal(H.shape) * 0.1
+    Wg = W * 0.5
+    a = oracle.flce(H, W, y)
+    b = oracle.flce(H, W, y, Hg=Hg, Wg=Wg)
+    assert b["loss"] == a["loss"]
+    np.testing.assert_array_equal(b["lse"], a["lse"])
+    np.testing.assert_allclose(b["dH"], a["dH"] * 0.5, rtol=1e-13, atol=1e-16)
+    # dW is linear in Hg: dW(Hg) - dW(H) = dW computed with (Hg - H)
+    c = oracle.flce(H, W, y, Hg=Hg - H, Wg=W)
+    np.testing.assert_allclose(b["dW"] - a["dW"], c["dW"], rtol=1e-10, atol=1e-14)
