@@ -18,9 +18,9 @@
 // 128 x 256 tile. kCta = 2: a cluster pair computes a 256 x 256 tile with
 // tcgen05 cta_group::2 MMAs; each CTA holds its 128 rows of A and 128 of the 256
 // rows of B, and its own 128 x 256 fp32 accumulator rows in TMEM.
-//   warp 0     : TMA producer (one thread of the even CTA of a pair) — streams
-//                A/B K-slices for both CTAs into a ring of shared-memory stages;
-//                all copies complete on the even CTA's barriers.
+//   warp 0     : TMA producer (one thread per CTA) — streams the CTA's A rows and
+//                B half, K-slice by K-slice, into a ring of shared-memory stages;
+//                the copies of both CTAs complete on the even CTA's stage barrier.
 //   warp 1     : TMEM allocator (both CTAs) and MMA issuer (one thread of the even
 //                CTA) — tcgen05.mma M x 256 x 16 steps into one of two TMEM
 //                accumulators.
@@ -200,8 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * kStages + a); };
   auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * kStages + 2 + a); };
   const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+  constexpr bool kCl = kCta == 2;  // waits acquire at cluster scope in pair mode
 
   if (threadIdx.x == 0) {
+    // full[s] of the even CTA counts the copies of both CTAs of a pair (the odd
+    // CTA's copies complete on it remotely); the odd CTA's full[s] is unused.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
@@ -232,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
-    // ---------------- TMA producer (the even CTA issues every copy of the pair) ------
-    if (lane == 0 && leader) {
+    // ---------------- TMA producer (each CTA loads its own A rows and B half) -----
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
@@ -245,48 +248,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
+            if (!mbar_wait_bounded<kCl>(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+            const uint32_t fb_local = full_bar(stage);
+            if (leader) mbar_arrive_expect_tx(fb_local, kCta * Cfg::kStageBytes);
+            // copies complete on the even CTA's barrier
+            const uint32_t fb = (kCta == 2) ? mapa_shared(fb_local, 0) : fb_local;
             const int kx = kb * (kFp8 ? 2 * BK : BK);  // elements per 128-byte row
+            const uint32_t sa = stage0 + stage * Cfg::kStageBytes;
+            const uint32_t sb = sa + Cfg::kABytes;
+            const int am = m_blk * Cfg::kTileM + static_cast<int>(rank) * BM;   // A rows
+            const int bn = n_blk * BN + static_cast<int>(rank) * Cfg::kBRows;   // B rows
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
+              if constexpr (kCta == 2) tma_load_2d_pair(dst, map, x, y, fb, pol);
+              else tma_load_2d_hint(dst, map, x, y, fb, pol);
+            };
+            auto load3 = [&](uint32_t dst, const CUtensorMap* map, int y, int z, uint64_t pol) {
+              if constexpr (kCta == 2) tma_load_3d_pair(dst, map, 0, y, z, fb, pol);
+              else tma_load_3d_hint(dst, map, 0, y, z, fb, pol);
+            };
+            if (!p.a_mn_major) {
+              load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
+            } else if (p.a_box3) {
+              load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
+            } else {
 #pragma unroll
-            for (int r = 0; r < kCta; ++r) {
-              const uint32_t sa_local = stage0 + stage * Cfg::kStageBytes;
-              const uint32_t sa = (kCta == 2) ? mapa_shared(sa_local, r) : sa_local;
-              const uint32_t sb = sa + Cfg::kABytes;
-              const int am = m_blk * Cfg::kTileM + r * BM;      // first A row of CTA r
-              const int bn = n_blk * BN + r * Cfg::kBRows;      // first B row of CTA r
-              auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
-                if constexpr (kCta == 2) tma_load_2d_pair(dst, map, x, y, fb, pol);
-                else tma_load_2d_hint(dst, map, x, y, fb, pol);
-              };
-              auto load3 = [&](uint32_t dst, const CUtensorMap* map, int y, int z, uint64_t pol) {
-                if constexpr (kCta == 2) tma_load_3d_pair(dst, map, 0, y, z, fb, pol);
-                else tma_load_3d_hint(dst, map, 0, y, z, fb, pol);
-              };
-              if (!p.a_mn_major) {
-                load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
-              } else if (p.a_box3) {
-                load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
-              } else {
-#pragma unroll
-                for (int j = 0; j < BM / 64; ++j)
-                  load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
-              }
-              if (!p.b_mn_major) {
-                load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
-              } else if (p.b_box3) {
-                load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
-              } else {
-#pragma unroll
-                for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                  load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
-              }
+              for (int j = 0; j < BM / 64; ++j)
+                load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
             }
-            issued_mask |= 1u << stage;
+            if (!p.b_mn_major) {
+              load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
+            } else if (p.b_box3) {
+              load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
+            } else {
+#pragma unroll
+              for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+            }
+      issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
               stage = 0;
@@ -299,12 +300,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
-      // Drain: every copy this thread issued (into either CTA) lands before the
-      // pair passes its final cluster barrier.
+      // Drain before the final barrier. The even CTA waits for every stage phase it
+      // armed; those phases count the odd CTA's copies too, and in a normal run the
+      // odd CTA issues exactly those phases. After an abort the odd CTA may have
+      // issued a phase the even CTA never armed, which it cannot observe: it then
+      // waits a bounded grace period (far longer than a copy takes) so that its
+      // copies land while both CTAs are still resident.
       const volatile int no_abort = 0;
-      for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s))
-          mbar_wait_bounded(full_bar(s), (issued_par >> s) & 1u, 1000000000ull, &no_abort);
+      if (leader) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait_bounded<kCl>(full_bar(s), (issued_par >> s) & 1u, 1000000000ull, &no_abort);
+      } else if (!ok || *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) {
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!mbar_wait_bounded(full_bar(stage), phase, tmo, abort_flag)) {
+            if (!mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag)) {
               ok = false;
               break;
             }
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
             }
             issued_any = true;
-            umma_commit_cg<kCta>(empty_bar(stage));
+            umma_commit_pair<kCta>(empty_bar(stage));  // frees the stage in both CTAs
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;

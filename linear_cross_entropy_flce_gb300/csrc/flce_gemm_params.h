@@ -23,13 +23,12 @@ constexpr uint32_t kMnBoxBytes = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major bo
 // instead of 48 KB, and the ring has 6 stages instead of 4.
 template <int kCta>
 struct TileCfg {
-  static constexpr int kStages = kCta == 2 ? 6 : 4;
+  static constexpr int kStages = kCta == 2 ? 7 : 4;
   static constexpr int kTileM = BM * kCta;         // rows of the tile (both CTAs)
   static constexpr int kBRows = BN / kCta;         // rows of B (tile columns) per CTA
   static constexpr uint32_t kABytes = BM * BK * 2;
   static constexpr uint32_t kBBytes = kBRows * BK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // per CTA
-  static constexpr uint32_t kTxBytes = kCta * kStageBytes;    // lands per stage on the pair
   static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
 };
 

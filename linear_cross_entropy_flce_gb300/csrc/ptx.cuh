@@ -51,20 +51,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// try_wait with cluster-scope acquire: for barriers that a peer CTA of the
-// cluster arrives on (or that a multicast tcgen05.commit completes).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Arrive on a barrier given by its shared::cluster address (possibly a peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
@@ -93,15 +79,35 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// try_wait with cluster-scope acquire: for barriers that a peer CTA of the
+// cluster arrives on (or that a multicast tcgen05.commit completes).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up (returns
 // false) when `timeout_ns` has elapsed or when another role of the CTA has set
 // the abort word, so that no wait in these kernels can spin forever.
+// kCluster = true acquires at cluster scope (barriers that a peer CTA of the
+// cluster arrives on, or that a multicast tcgen05.commit completes).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                                   const volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > timeout_ns) return false;
   }
