@@ -57,11 +57,11 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel: str, workload: str):
+def measured_traffic(kernel: str, workload: str, v_chunk: int):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary (profiles/dram_traffic_*.md lines 'traffic kernel=... workload=...
-    bytes_per_launch=... kernel_sha=...'); None when absent or when the kernel
-    sources changed since the counters were taken."""
+    v_chunk=... bytes_per_launch=... kernel_sha=...'); None when absent, when the
+    plan differs, or when the kernel sources changed since the counters were taken."""
     import glob
     sha = kernel_source_sha()
     for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
@@ -71,7 +71,7 @@ def measured_traffic(kernel: str, workload: str):
                     continue
                 kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
                 if kv.get("kernel") == kernel and kv.get("workload") == workload \
-                        and kv.get("kernel_sha") == sha:
+                        and kv.get("kernel_sha") == sha and kv.get("v_chunk") == str(v_chunk):
                     return float(kv["bytes_per_launch"])
     return None
 
@@ -584,7 +584,7 @@ def main(argv=None) -> int:
         "launches_per_step": f32_launches // args.steps,
         "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / args.steps),
         "ms_per_launch_avg": (per_kind["dw_gemm"] + per_kind["dh_gemm"]) / max(f32_launches, 1),
-        "traffic": measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name),
+        "traffic": measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name, plan["v_chunk"]),
         "traffic_source": "profiles/dram_traffic_*.md (ncu dram__bytes_read.sum + "
                           "dram__bytes_write.sum per launch; null if the kernel changed)",
         "kernel_sha": kernel_source_sha(),

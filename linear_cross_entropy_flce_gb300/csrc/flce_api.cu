@@ -166,36 +166,21 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
   if (o.v_chunk < 0 || o.n_block < 0) return FLCE_ERR_OPTION;
   if (o.v_chunk > 0 && o.v_chunk % BN != 0) return FLCE_ERR_OPTION;
   if (o.n_block > 0 && o.n_block % BM != 0) return FLCE_ERR_OPTION;
-  // Planned G chunk: at most kGChunkCapBytes and at most an eighth of the
-  // vocabulary (but never below 2048 ids), balanced so that the chunks have
-  // nearly equal length. All tokens form one block unless that would push the
-  // chunk below 2048 ids.
+  // Planned G chunk: vocabulary chunks of at most 16384 ids, balanced in length
+  // (a chunk's dH accumulation and launch ramp are paid per chunk, so fewer,
+  // longer chunks are faster); the tokens form one block unless one chunk of G
+  // would exceed kGChunkCapBytes, in which case they are split into equal
+  // blocks of whole 256-row pair tiles. Measured on GB300: long-sequence head
+  // 99.7 -> 93.9 ms with half the workspace, Llama-2-like head 1.93 -> 1.40 ms.
   int64_t cv = o.v_chunk, nb = o.n_block;
-  auto cv_for_rows = [&](int64_t rows) {
-    const int64_t r = ceil_div(rows, BM) * BM;
-    int64_t m = std::min<int64_t>(16384, static_cast<int64_t>(kGChunkCapBytes / (2 * r)));
-    m = std::min<int64_t>(m, std::max<int64_t>(2048, V / 8));
-    m = std::max<int64_t>(BN, m / BN * BN);
-    const int64_t chunks = ceil_div(V, m);
-    return ceil_div(ceil_div(V, chunks), BN) * BN;
-  };
-  auto nb_for_cv = [&](int64_t c) {
-    const int64_t r = static_cast<int64_t>(kGChunkCapBytes / (2 * c)) / BM * BM;
-    return std::max<int64_t>(BM, r);
-  };
-  if (cv == 0 && nb == 0) {
-    const int64_t r = ceil_div(N, BM) * BM;
-    if (static_cast<int64_t>(kGChunkCapBytes / (2 * r)) >= 2048) {
-      cv = cv_for_rows(N);
-      nb = N;
-    } else {
-      cv = 2048;
-      nb = nb_for_cv(cv);
-    }
-  } else if (cv == 0) {
-    cv = cv_for_rows(std::min(nb, N));
-  } else if (nb == 0) {
-    nb = nb_for_cv(cv);
+  if (cv == 0) {
+    const int64_t chunks = ceil_div(V, 16384);
+    cv = ceil_div(ceil_div(V, chunks), BN) * BN;
+  }
+  if (nb == 0) {
+    const int64_t bytes = ceil_div(N, BM * 2) * (BM * 2) * cv * 2;
+    const int64_t blocks = std::max<int64_t>(1, ceil_div(bytes, static_cast<int64_t>(kGChunkCapBytes)));
+    nb = blocks == 1 ? N : ceil_div(ceil_div(N, blocks), BM * 2) * (BM * 2);
   }
   cv = std::min(cv, v_round);
   nb = std::min(nb, N);

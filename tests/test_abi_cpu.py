@@ -43,18 +43,20 @@ def test_default_options():
 
 
 def test_workspace_is_far_below_logits():
-    # The bound is one G chunk plus small per-token arrays; at tile-sized
-    # problems the 128 x 256 tile rounding dominates instead.
+    # The bound is one G chunk (at most 16384 vocabulary ids x at most 256 MiB)
+    # plus small per-token arrays and one fp32 dH block; at tile-sized problems
+    # the 256 x 256 tile rounding dominates instead.
     assert flce.workspace_size(64, 128, 1000) < 1 << 20
-    for N, D, V in [(4096, 2048, 32000), (8192, 4096, 128256),
-                    (16384, 3584, 152064), (32768, 4096, 128256)]:
+    for N, D, V, frac in [(4096, 2048, 32000, 0.35), (8192, 4096, 128256, 0.11),
+                          (16384, 3584, 152064, 0.05), (32768, 4096, 128256, 0.03)]:
         ws = flce.workspace_size(N, D, V)
-        assert 0 < ws < N * V * 4 / 4, (N, D, V, ws)
+        assert 0 < ws < N * V * 4 * frac, (N, D, V, ws)
+        assert ws < 600 << 20
 
 
 def test_workspace_grows_with_requested_chunk():
-    a = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=4096))
-    b = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=16384))
+    a = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=4096, n_block=8192))
+    b = flce.workspace_size(8192, 4096, 128256, flce.make_options(v_chunk=16384, n_block=8192))
     assert b - a == pytest.approx(8192 * (16384 - 4096) * 2, rel=0.01)
 
 
