@@ -240,6 +240,20 @@ int flce_ce_logits(const void* logits, int32_t dtype, int64_t ld, const int32_t*
                    void* stream);
 
 /*
+ * Multiply dH (bf16, dh_elems elements) and dW (dw_dtype, dw_elems elements) in
+ * place by the fp32 device scalar *scale, on `stream`. This is the backward step
+ * of the drop-in loss (GPU MODE lecture 28 notes, cross-entropy section: the
+ * fused loss replaces PyTorch's loss module, so autograd hands it dL/dloss):
+ * flce_forward_backward computes the gradients for dL/dloss = 1, and this call
+ * applies the actual upstream factor. When *scale == 1 the kernels exit without
+ * touching memory (no host synchronisation is needed to find that out). Either
+ * buffer may be NULL with 0 elements; sizes in bytes must be multiples of 16 and
+ * pointers 16-byte aligned.
+ */
+int flce_scale_grads(uint16_t* dH, int64_t dh_elems, void* dW, int64_t dw_elems,
+                     int32_t dw_dtype, const float* scale, void* stream);
+
+/*
  * Synchronise `stream`, read the device status word and return it (FLCE_OK, or
  * the first device error a call recorded). Returns FLCE_ERR_CUDA if the stream
  * reports a CUDA error. status == NULL returns FLCE_OK after the synchronisation.

@@ -9,10 +9,14 @@ from ._binding import (FLCE_ERR_ALIGN, FLCE_ERR_CUDA, FLCE_ERR_DEVICE, FLCE_ERR_
                        FLCE_ERR_NULL, FLCE_ERR_OPTION, FLCE_ERR_SHAPE, FLCE_ERR_TIMEOUT,
                        FLCE_ERR_WORKSPACE, FLCE_OK, FLCEError, LIB_PATH, Options, Result,
                        ce_logits, check_status, forward, forward_backward, forward_backward_fp8, get_plan, lib, make_options,
-                       status_string, workspace_size)
+                       scale_grads, status_string, workspace_size)
+from .loss import (FusedLinearCrossEntropyFunction, FusedLinearCrossEntropyLoss,
+                   fused_linear_cross_entropy)
 
 __all__ = ["FLCE_ERR_ALIGN", "FLCE_ERR_CUDA", "FLCE_ERR_DEVICE", "FLCE_ERR_LABEL_RANGE",
            "FLCE_ERR_NULL", "FLCE_ERR_OPTION", "FLCE_ERR_SHAPE", "FLCE_ERR_TIMEOUT",
            "FLCE_ERR_WORKSPACE", "FLCE_OK", "FLCEError", "LIB_PATH", "Options", "Result",
            "ce_logits", "check_status", "forward", "forward_backward", "forward_backward_fp8", "get_plan", "lib", "make_options",
-           "status_string", "workspace_size"]
+           "scale_grads", "status_string", "workspace_size",
+           "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
+           "fused_linear_cross_entropy"]

@@ -97,6 +97,8 @@ lib.flce_forward_backward_fp8.argtypes = [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _
                                           ctypes.POINTER(Options), _vp, _vp, _vp, _vp, _vp,
                                           ctypes.c_size_t, _vp, _vp]
 lib.flce_forward_backward_fp8.restype = ctypes.c_int
+lib.flce_scale_grads.argtypes = [_vp, _i64, _vp, _i64, ctypes.c_int32, _vp, _vp]
+lib.flce_scale_grads.restype = ctypes.c_int
 lib.flce_check_status.argtypes = [_vp, _vp]
 lib.flce_check_status.restype = ctypes.c_int
 lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -374,6 +376,21 @@ def forward_backward_fp8(H8, scale_h: float, W8, scale_w: float, labels, H=None,
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_forward_backward_fp8" if grads else "flce_forward_fp8")
     return Result(loss, lse, dH if need_dh else None, dW if need_dw else None, status)
+
+
+def scale_grads(dH, dW, scale, stream=None) -> None:
+    """dH *= scale and dW *= scale in place (flce_scale_grads); scale is a
+    one-element float32 CUDA tensor. Either gradient may be None."""
+    import torch
+    if scale.dtype != torch.float32 or scale.numel() != 1 or not scale.is_cuda:
+        raise TypeError("scale must be a one-element float32 CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(scale.device).cuda_stream
+    dw_dtype = DW_DTYPES["bfloat16" if (dW is not None and dW.dtype == torch.bfloat16) else "float32"]
+    rc = lib.flce_scale_grads(_ptr(dH), dH.numel() if dH is not None else 0, _ptr(dW),
+                              dW.numel() if dW is not None else 0, dw_dtype, _ptr(scale), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_scale_grads")
 
 
 def check_status(status, stream=None) -> int:

@@ -715,6 +715,30 @@ int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W
                    status, stream);
 }
 
+int flce_scale_grads(uint16_t* dH, int64_t dh_elems, void* dW, int64_t dw_elems,
+                     int32_t dw_dtype, const float* scale, void* stream) {
+  if (scale == nullptr) return FLCE_ERR_NULL;
+  if (dh_elems < 0 || dw_elems < 0) return FLCE_ERR_SHAPE;
+  if ((dH == nullptr && dh_elems > 0) || (dW == nullptr && dw_elems > 0)) return FLCE_ERR_NULL;
+  if (dw_dtype != FLCE_DTYPE_F32 && dw_dtype != FLCE_DTYPE_BF16) return FLCE_ERR_OPTION;
+  const int64_t dw_bytes = dw_elems * (dw_dtype == FLCE_DTYPE_BF16 ? 2 : 4);
+  if ((dh_elems * 2) % 16 != 0 || dw_bytes % 16 != 0) return FLCE_ERR_ALIGN;
+  if ((dH && !flce::aligned16(dH)) || (dW && !flce::aligned16(dW)) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return FLCE_ERR_ALIGN;
+  int sms = 0;
+  const int rc = flce::device_info(&sms);
+  if (rc != FLCE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dh_elems > 0 && flce::launch_scale(dH, dh_elems * 2, 1, scale, sms, st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (dw_elems > 0 &&
+      flce::launch_scale(dW, dw_bytes, dw_dtype == FLCE_DTYPE_BF16 ? 1 : 0, scale, sms, st) !=
+          cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
+
 int flce_check_status(const int32_t* status, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;

@@ -45,4 +45,8 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
                            float* nll, void* g, int64_t gld_bytes, int sms,
                            cudaStream_t stream);
 
+// x (bf16 if bf16, else fp32; bytes a multiple of 16) *= *scale, in place.
+cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, int sms,
+                         cudaStream_t stream);
+
 }  // namespace flce

@@ -99,7 +99,47 @@ __global__ void __launch_bounds__(kReduceThreads)
   }
 }
 
+// x *= *scale over n16 16-byte vectors (bf16 or fp32), in place. Every thread
+// reads the scale first and leaves at once when it is exactly 1.
+template <int kBf16>
+__global__ void scale_kernel(uint4* __restrict__ x, int64_t n16, const float* __restrict__ scale) {
+  const float sc = *scale;
+  if (sc == 1.0f) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    uint4 v = x[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (kBf16) {
+        const float lo = __uint_as_float(w[k] << 16) * sc;
+        const float hi = __uint_as_float(w[k] & 0xFFFF0000u) * sc;
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        w[k] = r;
+      } else {
+        w[k] = __float_as_uint(__uint_as_float(w[k]) * sc);
+      }
+    }
+    x[i] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, int sms,
+                         cudaStream_t stream) {
+  const int64_t n16 = bytes / 16;
+  if (n16 <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (n16 + threads - 1) / threads;
+  const int grid = static_cast<int>(want < static_cast<int64_t>(sms) * 8 ? want : static_cast<int64_t>(sms) * 8);
+  if (bf16)
+    scale_kernel<1><<<grid, threads, 0, stream>>>(static_cast<uint4*>(x), n16, scale);
+  else
+    scale_kernel<0><<<grid, threads, 0, stream>>>(static_cast<uint4*>(x), n16, scale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
                              int V, int part_stride, int splits, int ignore_index, float* lse,

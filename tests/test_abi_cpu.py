@@ -24,8 +24,8 @@ def test_header_declares_the_abi():
     assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
                             "flce_ce_workspace_size", "flce_ce_logits", "flce_forward_fp8",
-                            "flce_forward_backward_fp8", "flce_check_status",
-                            "flce_status_string"])
+                            "flce_forward_backward_fp8", "flce_scale_grads",
+                            "flce_check_status", "flce_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -159,6 +159,15 @@ def test_fp8_host_rejections():
     # the gradient products need the bf16 operands
     assert g(0x1000, 1.0, 0x2000, 1.0, None, None, 0x3000, 64, 128, 1000, None, 0x4000, None,
              0x6000, 0x7000, 0x5000, 1 << 30, None, None) == flce.FLCE_ERR_NULL
+
+
+def test_scale_grads_host_rejections():
+    f = flce.lib.flce_scale_grads
+    assert f(0x1000, 8, None, 0, 0, None, None) == flce.FLCE_ERR_NULL
+    assert f(None, 8, None, 0, 0, 0x2000, None) == flce.FLCE_ERR_NULL
+    assert f(0x1000, 4, None, 0, 0, 0x2000, None) == flce.FLCE_ERR_ALIGN   # 8 bytes of bf16
+    assert f(0x1000, 8, 0x3000, 8, 5, 0x2000, None) == flce.FLCE_ERR_OPTION
+    assert f(0x1000, -8, None, 0, 0, 0x2000, None) == flce.FLCE_ERR_SHAPE
 
 
 def test_status_strings():
