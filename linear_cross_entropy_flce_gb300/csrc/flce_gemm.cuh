@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   using Cfg = TileCfg<kCta>;
   constexpr int kStages = Cfg::kStages;
+  constexpr int kSub = Cfg::kSub;
+  const int k_stages = (p.k_blocks + kSub - 1) / kSub;  // ring stages per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -247,18 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m_blk, n_begin, n_end;
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
+          for (int ks = 0; ks < k_stages; ++ks) {
             if (!mbar_wait_bounded<kCl>(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
               ok = false;
               break;
             }
+            const int nsub = min(kSub, p.k_blocks - ks * kSub);
             const uint32_t fb_local = full_bar(stage);
-            if (leader) mbar_arrive_expect_tx(fb_local, kCta * Cfg::kStageBytes);
+            if (leader)
+              mbar_arrive_expect_tx(fb_local, static_cast<uint32_t>(kCta * nsub) * Cfg::kSubBytes);
             // copies complete on the even CTA's barrier
             const uint32_t fb = (kCta == 2) ? mapa_shared(fb_local, 0) : fb_local;
-            const int kx = kb * (kFp8 ? 2 * BK : BK);  // elements per 128-byte row
-            const uint32_t sa = stage0 + stage * Cfg::kStageBytes;
-            const uint32_t sb = sa + Cfg::kABytes;
             const int am = m_blk * Cfg::kTileM + static_cast<int>(rank) * BM;   // A rows
             const int bn = n_blk * BN + static_cast<int>(rank) * Cfg::kBRows;   // B rows
             auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
@@ -269,25 +270,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (kCta == 2) tma_load_3d_pair(dst, map, 0, y, z, fb, pol);
               else tma_load_3d_hint(dst, map, 0, y, z, fb, pol);
             };
-            if (!p.a_mn_major) {
-              load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
-            } else if (p.a_box3) {
-              load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
-            } else {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j)
-                load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
-            }
-            if (!p.b_mn_major) {
-              load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
-            } else if (p.b_box3) {
-              load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
-            } else {
+            for (int sub = 0; sub < kSub; ++sub) {
+              if (sub >= nsub) break;
+              const int kx = (ks * kSub + sub) * (kFp8 ? 2 * BK : BK);  // elements per 128-byte row
+              const uint32_t sa = stage0 + stage * Cfg::kStageBytes + sub * Cfg::kSubBytes;
+              const uint32_t sb = sa + Cfg::kABytes;
+              if (!p.a_mn_major) {
+                load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
+              } else if (p.a_box3) {
+                load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
+              } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+                for (int j = 0; j < BM / 64; ++j)
+                  load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
+              }
+              if (!p.b_mn_major) {
+                load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
+              } else if (p.b_box3) {
+                load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
+              } else {
+#pragma unroll
+                for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                  load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+              }
             }
-      issued_mask |= 1u << stage;
+            issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
               stage = 0;
@@ -351,22 +359,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
+          for (int ks = 0; ks < k_stages; ++ks) {
             if (!mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sa = stage0 + stage * Cfg::kStageBytes;
-            const uint32_t sb = sa + Cfg::kABytes;
+            const int nsub = min(kSub, p.k_blocks - ks * kSub);
 #pragma unroll
-            for (int k = 0; k < BK / UK; ++k) {
-              const uint64_t da = a_mn ? make_sw128_desc(sa + k * (UK * 128), kMnBoxBytes, 1024)
-                                       : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
-              const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
-                                       : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
-              if constexpr (kFp8) umma_f8_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
-              else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int sub = 0; sub < kSub; ++sub) {
+              if (sub >= nsub) break;
+              const uint32_t sa = stage0 + stage * Cfg::kStageBytes + sub * Cfg::kSubBytes;
+              const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+              for (int k = 0; k < BK / UK; ++k) {
+                const uint64_t da = a_mn ? make_sw128_desc(sa + k * (UK * 128), kMnBoxBytes, 1024)
+                                         : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
+                const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
+                                         : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
+                const uint32_t accum = (ks | sub | k) != 0 ? 1u : 0u;
+                if constexpr (kFp8) umma_f8_cg<kCta>(d_tmem, da, db, p.idesc, accum);
+                else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, accum);
+              }
             }
             issued_any = true;
             umma_commit_pair<kCta>(empty_bar(stage));  // frees the stage in both CTAs

@@ -19,16 +19,23 @@ constexpr uint32_t kMnBoxBytes = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major bo
 
 // Tile configuration. kCta = 1: one CTA computes a 128 x 256 tile. kCta = 2: a
 // cluster pair computes a 256 x 256 tile with tcgen05 cta_group::2; each CTA holds
-// its 128 rows of A and half (128 rows) of B, so each SM stages 32 KB per K step
-// instead of 48 KB, and the ring has 6 stages instead of 4.
+// its 128 rows of A and half (128 rows) of B, so each SM stages 32 KB per 64-deep K
+// block instead of 48 KB.
+// A ring stage holds kSub consecutive K blocks under one full/empty barrier pair.
+// The MMA thread's wait and commit per stage cost about as much as one MMA, and the
+// tensor pipe queues little work ahead, so with cta_group::2 two K blocks (eight
+// MMAs) share each wait and commit; three 64 KB stages keep as many bytes in flight
+// as six 32 KB ones.
 template <int kCta>
 struct TileCfg {
-  static constexpr int kStages = kCta == 2 ? 7 : 4;
+  static constexpr int kSub = kCta == 2 ? 2 : 1;   // K blocks per ring stage
+  static constexpr int kStages = kCta == 2 ? 3 : 4;
   static constexpr int kTileM = BM * kCta;         // rows of the tile (both CTAs)
   static constexpr int kBRows = BN / kCta;         // rows of B (tile columns) per CTA
   static constexpr uint32_t kABytes = BM * BK * 2;
   static constexpr uint32_t kBBytes = kBRows * BK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // per CTA
+  static constexpr uint32_t kSubBytes = kABytes + kBBytes;    // one K block, per CTA
+  static constexpr uint32_t kStageBytes = kSub * kSubBytes;   // one ring stage, per CTA
   static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
 };
 
