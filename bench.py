@@ -500,8 +500,12 @@ def main(argv=None) -> int:
     for e in evs:
         e.record(stream)  # creates the event handles
     torch.cuda.synchronize(dev)
-    kinds = ["lse_gemm", "lse_merge", "loss_reduce"] + \
-        ["grad_gemm", "dw_gemm", "dh_gemm"] * (plan["n_blocks"] * plan["n_chunks"])
+    # per token block: each chunk's three GEMMs, then (several chunks) the bf16
+    # rounding of the block's fp32 dH accumulator
+    per_block = ["grad_gemm", "dw_gemm", "dh_gemm"] * plan["n_chunks"] + \
+        (["dh_round"] if plan["n_chunks"] > 1 else [])
+    kinds = ["lse_gemm", "lse_merge", "loss_reduce"] + per_block * plan["n_blocks"]
+    assert len(kinds) == n_launch, (len(kinds), n_launch)
     per_kind = {k: 0.0 for k in kinds}
     n_kind = {k: 0 for k in kinds}
     for _ in range(args.steps):
@@ -593,7 +597,7 @@ def main(argv=None) -> int:
                         "tflops": rate(kernel_ms[k]) if k.endswith("gemm") else None,
                         "share": kernel_ms[k] / sum(kernel_ms.values())}
                     for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dw_gemm",
-                              "dh_gemm"]},
+                              "dh_gemm", "dh_round"] if k in kernel_ms},
     }
     clocks = clk.summary()
 

@@ -98,6 +98,26 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   return r == CUDA_SUCCESS;
 }
 
+// Output map of the GEMM epilogue's TMA stores: [rows][cols] row-major with row
+// stride ld elements, boxes of 32 x 32; fp32 boxes use the 128-byte swizzle and
+// bf16 boxes the 64-byte one (the layouts the epilogue stages in shared memory).
+// Stores outside [rows) x [cols) are dropped, which clips ragged tiles.
+bool encode_out(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64_t rows,
+                uint64_t ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint64_t esz = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * esz};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tiles are computed by cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int kCtaGroup = 2;
 
@@ -389,7 +409,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   const int64_t rows_b = ceil_div(P.n_block, P.tile_m) * P.tile_m;
   // MN-major operands: one 3-D copy per CTA when the MN extent is a multiple of
   // 64 (always for the G chunk), else 64-wide 2-D boxes.
-  CUtensorMap mH_mn, mW_mn, mG_mn, mG_k;
+  CUtensorMap mH_mn, mW_mn, mG_mn, mG_k, mG_out;
   const bool d_box3 = D % 64 == 0;
   const uint32_t b_chunks = static_cast<uint32_t>(BN / cta / 64);
   const bool ok_h = d_box3 ? encode_bf16_mn3(&mH_mn, H, D, N, D, BK, b_chunks)
@@ -397,9 +417,13 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   const bool ok_w = d_box3 ? encode_bf16_mn3(&mW_mn, W, D, V, D, BK, b_chunks)
                            : encode_bf16(&mW_mn, W, D, V, D, 64, BK);
   if (!ok_h || !ok_w || !encode_bf16_mn3(&mG_mn, G, P.v_chunk, rows_b, P.v_chunk, BK, BM / 64) ||
-      !encode_bf16(&mG_k, G, P.v_chunk, rows_b, P.v_chunk, BK, BM))
+      !encode_bf16(&mG_k, G, P.v_chunk, rows_b, P.v_chunk, BK, BM) ||
+      !encode_out(&mG_out, G, true, P.v_chunk, rows_b, P.v_chunk))
     return FLCE_ERR_CUDA;
   const bool dw_bf16 = o.dw_dtype == FLCE_DTYPE_BF16;
+  // dW goes to fp32 dW, to bf16 dW (one token block), or to the fp32 accumulator
+  // that bf16 dW is rounded from after the last token block.
+  const bool dw_direct_bf16 = dw_bf16 && P.n_nblocks == 1;
 
   for (int b = 0; b < P.n_nblocks; ++b) {
     const int64_t b0 = static_cast<int64_t>(b) * P.n_block;
@@ -431,9 +455,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
       q.ignore_index = o.ignore_index;
       q.lse = lse;
       q.scale = scal;
-      q.g_out = G;
-      q.g_ld = P.v_chunk;
-      if (launch_gemm_grad(cta, mH_k, mW_k, q, cta * std::min(q.num_units, pairs), st,
+      q.out_row0 = 0;
+      if (launch_gemm_grad(cta, mH_k, mW_k, mG_out, q, cta * std::min(q.num_units, pairs), st,
                            fp8 ? 1 : 0) !=
               cudaSuccess ||
           !trace())
@@ -457,27 +480,16 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         w.status = status;
         w.m_valid = c_len;
         w.n_valid = static_cast<int>(D);
-        const bool first = b == 0, last = b == P.n_nblocks - 1;
-        if (!dw_bf16) {
-          w.out_f32 = static_cast<float*>(dW);
-          w.out_f32_ld = D;
-          w.out_f32_row0 = static_cast<int>(c0);
-          w.out_mode = first ? OUT_STORE_F32 : OUT_ADD_F32;
-        } else if (P.n_nblocks == 1) {
-          w.out_bf16 = static_cast<uint16_t*>(dW);
-          w.out_bf16_ld = D;
-          w.out_bf16_row0 = static_cast<int>(c0);
-          w.out_mode = OUT_STORE_BF16;
-        } else {
-          w.out_f32 = dw_acc;
-          w.out_f32_ld = D;
-          w.out_f32_row0 = static_cast<int>(c0);
-          w.out_bf16 = static_cast<uint16_t*>(dW);
-          w.out_bf16_ld = D;
-          w.out_bf16_row0 = static_cast<int>(c0);
-          w.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
-        }
-        if (launch_gemm_f32(cta, mG_mn, mH_mn, w, cta * std::min(w.num_units, pairs), st) !=
+        // the map holds exactly the chunk's rows, so ragged tiles are clipped
+        CUtensorMap mDW;
+        const int64_t dw_off = c0 * D;
+        void* dw_base = dw_direct_bf16 ? static_cast<void*>(static_cast<uint16_t*>(dW) + dw_off)
+                        : dw_bf16      ? static_cast<void*>(dw_acc + dw_off)
+                                       : static_cast<void*>(static_cast<float*>(dW) + dw_off);
+        if (!encode_out(&mDW, dw_base, dw_direct_bf16, D, c_len, D)) return FLCE_ERR_CUDA;
+        w.out_row0 = 0;
+        w.out_mode = dw_direct_bf16 ? OUT_STORE_BF16 : (b == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
+        if (launch_gemm_f32(cta, mG_mn, mH_mn, mDW, w, cta * std::min(w.num_units, pairs), st) !=
                 cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;
@@ -500,24 +512,32 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         h.status = status;
         h.m_valid = nb_len;
         h.n_valid = static_cast<int>(D);
-        const bool first = c == 0, last = c == P.n_chunks - 1;
-        h.out_f32 = dh_acc;
-        h.out_f32_ld = D;
-        h.out_f32_row0 = 0;
-        h.out_bf16 = dH;
-        h.out_bf16_ld = D;
-        h.out_bf16_row0 = static_cast<int>(b0);
-        if (P.n_chunks == 1)
-          h.out_mode = OUT_STORE_BF16;
-        else
-          h.out_mode = first ? OUT_STORE_F32 : (last ? OUT_ADD_TO_BF16 : OUT_ADD_F32);
-        if (launch_gemm_f32(cta, mG_k, mW_mn, h, cta * std::min(h.num_units, pairs), st) !=
+        // one chunk: bf16 dH directly; else an fp32 accumulator of this token
+        // block's rows (stored by chunk 0, reduce-added by the others), rounded
+        // to bf16 after the last chunk. The map holds exactly the block's rows.
+        CUtensorMap mDH;
+        const bool dh_direct = P.n_chunks == 1;
+        if (!(dh_direct ? encode_out(&mDH, dH + b0 * D, true, D, nb_len, D)
+                        : encode_out(&mDH, dh_acc, false, D, nb_len, D)))
+          return FLCE_ERR_CUDA;
+        h.out_row0 = 0;
+        h.out_mode = dh_direct ? OUT_STORE_BF16 : (c == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
+        if (launch_gemm_f32(cta, mG_k, mW_mn, mDH, h, cta * std::min(h.num_units, pairs), st) !=
                 cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;
       }
     }
+    if (dH != nullptr && P.n_chunks > 1 &&
+        (launch_f32_to_bf16(dh_acc, dH + b0 * D, static_cast<int64_t>(nb_len) * D, sms, st) !=
+             cudaSuccess ||
+         !trace()))
+      return FLCE_ERR_CUDA;
   }
+  if (dW != nullptr && dw_bf16 && !dw_direct_bf16 &&
+      (launch_f32_to_bf16(dw_acc, static_cast<uint16_t*>(dW), V * D, sms, st) != cudaSuccess ||
+       !trace()))
+    return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
 
@@ -583,9 +603,14 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
   info->n_blocks = P.n_nblocks;
   info->n_chunks = P.n_chunks;
   info->v_splits = P.splits;
+  // LSE GEMM, merge, reduce; per token block: per chunk the gradient GEMM and
+  // the dW / dH GEMMs asked for, then (several chunks) the bf16 rounding of dH;
+  // bf16 dW over several token blocks: one rounding of its accumulator at the end.
   const int per_chunk = 1 + (want_dh ? 1 : 0) + (want_dw ? 1 : 0);
+  const int per_block = P.n_chunks * per_chunk + ((want_dh && P.n_chunks > 1) ? 1 : 0);
+  const bool dw_round = want_dw && o.dw_dtype == FLCE_DTYPE_BF16 && P.n_nblocks > 1;
   info->kernel_launches =
-      3 + ((want_dh || want_dw) ? P.n_nblocks * P.n_chunks * per_chunk : 0);
+      3 + ((want_dh || want_dw) ? P.n_nblocks * per_block + (dw_round ? 1 : 0) : 0);
   info->workspace_bytes = ws;
   info->plan_bytes = P.total;
   return FLCE_OK;

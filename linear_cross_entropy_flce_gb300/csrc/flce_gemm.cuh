@@ -115,11 +115,34 @@ __device__ __forceinline__ void lse_chunk(const float (&v)[32], int col_local, i
   st.m = mn;
 }
 
-// G for one 32-column chunk: bf16 (exp(z - lse) - [v = y]) * sc; 0 past n_valid.
+// Epilogue staging. Each epilogue warp writes its 32 rows x 32 columns into a
+// shared-memory box in the layout the output map's swizzle expects, then one lane
+// hands the box to a TMA store: the global writes leave the SM as whole lines
+// instead of one 16-byte piece of 32 different rows per store instruction.
+//   fp32 box: rows of 128 bytes, 128-byte swizzle: 16-byte chunk q of row r sits
+//             at chunk q ^ (r % 8);
+//   bf16 box: rows of 64 bytes, 64-byte swizzle: chunk q of row r at q ^ ((r / 2) % 4).
+__device__ __forceinline__ void stage_f32_row(uint32_t box, int r, const float (&v)[32]) {
+  const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(row + ((static_cast<uint32_t>(q ^ (r & 7))) << 4), __float_as_uint(v[4 * q]),
+                 __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                 __float_as_uint(v[4 * q + 3]));
+}
+
+__device__ __forceinline__ void stage_bf16_row(uint32_t box, int r, const float (&v)[32]) {
+  const uint32_t row = box + static_cast<uint32_t>(r) * 64u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(row + ((static_cast<uint32_t>(q ^ ((r >> 1) & 3))) << 4),
+                 pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                 pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// G for one 32-column chunk: (exp(z - lse) - [v = y]) * sc, 0 past n_valid.
 __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, int n_valid,
-                                           int rel_target, float nlse2, float sc,
-                                           uint16_t* gdst) {
-  float g[32];
+                                           int rel_target, float nlse2, float sc, float (&g)[32]) {
 #pragma unroll
   for (int k = 0; k < 32; ++k) g[k] = ex2_approx(fmaf(v[k], kLog2e, nlse2)) * sc;
   if (static_cast<unsigned>(rel_target) < 32u) {
@@ -132,41 +155,6 @@ __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, 
     for (int k = 0; k < 32; ++k)
       if (col_local + k >= n_valid) g[k] = 0.f;
   }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    st_global_v4(gdst + q * 8, pack_bf16x2(g[q * 8 + 0], g[q * 8 + 1]),
-                 pack_bf16x2(g[q * 8 + 2], g[q * 8 + 3]), pack_bf16x2(g[q * 8 + 4], g[q * 8 + 5]),
-                 pack_bf16x2(g[q * 8 + 6], g[q * 8 + 7]));
-  }
-}
-
-__device__ __forceinline__ void f32_chunk(const float (&v)[32], const GemmParams& p, int row,
-                                          int col) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int c = col + 4 * j;
-    if (c >= p.n_valid) break;
-    float a = v[4 * j + 0], b = v[4 * j + 1], cc = v[4 * j + 2], d = v[4 * j + 3];
-    if (p.out_mode == OUT_STORE_F32 || p.out_mode == OUT_ADD_F32) {
-      float* dst = p.out_f32 + static_cast<int64_t>(p.out_f32_row0 + row) * p.out_f32_ld + c;
-      if (p.out_mode == OUT_ADD_F32) {
-        const float4 o = ld_global_v4f(dst);
-        a += o.x; b += o.y; cc += o.z; d += o.w;
-      }
-      st_global_v4(dst, __float_as_uint(a), __float_as_uint(b), __float_as_uint(cc),
-                   __float_as_uint(d));
-    } else {
-      if (p.out_mode == OUT_ADD_TO_BF16) {
-        const float* src =
-            p.out_f32 + static_cast<int64_t>(p.out_f32_row0 + row) * p.out_f32_ld + c;
-        const float4 o = ld_global_v4f(src);
-        a += o.x; b += o.y; cc += o.z; d += o.w;
-      }
-      uint16_t* dst = p.out_bf16 + static_cast<int64_t>(p.out_bf16_row0 + row) * p.out_bf16_ld + c;
-      const uint32_t lo = pack_bf16x2(a, b), hi = pack_bf16x2(cc, d);
-      asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(dst), "r"(lo), "r"(hi) : "memory");
-    }
-  }
 }
 
 // ---- the kernel --------------------------------------------------------------------
@@ -177,7 +165,8 @@ __device__ __forceinline__ void f32_chunk(const float (&v)[32], const GemmParams
 template <int kEpi, int kCta, int kFp8 = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using Cfg = TileCfg<kCta>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kSub = Cfg::kSub;
@@ -185,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kRingBytes + 8 * Cfg::kStgBytes);
   // bars: full[kStages] | empty[kStages] | tfull[2] | tempty[2] | drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -222,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (kEpi != EPI_LSE) tma_prefetch_desc(&tmC);
   }
   // Barriers of both CTAs are initialised before either CTA touches the other's.
   if constexpr (kCta == 2) cluster_sync();
@@ -421,6 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float scale_v = 0.f;
     if constexpr (kEpi == EPI_GRAD) scale_v = *p.scale;
+    // this warp's two staging boxes, used alternately
+    const uint32_t stg = stage0 + Cfg::kRingBytes + static_cast<uint32_t>(quarter) * 2u * Cfg::kStgBytes;
+    uint32_t nbox = 0;
     for (int u = pair; ok && u < p.num_units; u += num_pairs) {
       int m_blk, n_begin, n_end;
       const int col_unit = unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
@@ -480,11 +473,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col = n_blk * BN + c * 32;  // product column
           if constexpr (kEpi == EPI_LSE) {
             lse_chunk(v, col, p.n_valid, y - (p.col_base + col), st);
-          } else if constexpr (kEpi == EPI_GRAD) {
-            grad_chunk(v, col, p.n_valid, y - (p.col_base + col), nlse2, sc,
-                       p.g_out + static_cast<int64_t>(prow) * p.g_ld + col);
           } else {
-            if (row_ok && col < p.n_valid) f32_chunk(v, p, prow, col);
+            const uint32_t box = stg + (nbox & 1u) * Cfg::kStgBytes;
+            // the store issued two boxes ago from this buffer has read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            if constexpr (kEpi == EPI_GRAD) {
+              float g[32];
+              grad_chunk(v, col, p.n_valid, y - (p.col_base + col), nlse2, sc, g);
+              stage_bf16_row(box, lane, g);
+            } else if (p.out_mode == OUT_STORE_BF16) {
+              stage_bf16_row(box, lane, v);
+            } else {
+              stage_f32_row(box, lane, v);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              // rows and columns outside the map are dropped by the store
+              const int oy = p.out_row0 + m_blk * Cfg::kTileM + static_cast<int>(rank) * BM +
+                             quarter * 32;
+              if (kEpi == EPI_F32 && p.out_mode == OUT_ADD_F32) tma_reduce_add_2d(&tmC, box, col, oy);
+              else tma_store_2d(&tmC, box, col, oy);
+              bulk_commit_group();
+            }
+            ++nbox;
           }
         }
         tc_fence_before();
@@ -511,6 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       if (lane == 0) record_status(p.status, kStatusTimeout);
       *abort_flag = 1;
+    }
+    // every store of this warp has landed before the CTA can exit
+    if constexpr (kEpi != EPI_LSE) {
+      if (lane == 0) bulk_wait_group_all();
+      __syncwarp();
     }
   }
 

@@ -7,8 +7,8 @@ namespace flce {
 namespace {
 
 template <int kCta>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                   const GemmParams& p, int grid, cudaStream_t stream) {
   auto kern = flce_gemm_kernel<EPI_F32, kCta, 0>;
   constexpr size_t smem = TileCfg<kCta>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -26,14 +26,15 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                           const GemmParams& p, int grid, cudaStream_t stream) {
-  return cta_group == 2 ? launch<2>(a, b, p, grid, stream) : launch<1>(a, b, p, grid, stream);
+                            const CUtensorMap& c, const GemmParams& p, int grid,
+                            cudaStream_t stream) {
+  return cta_group == 2 ? launch<2>(a, b, c, p, grid, stream) : launch<1>(a, b, c, p, grid, stream);
 }
 
 }  // namespace flce

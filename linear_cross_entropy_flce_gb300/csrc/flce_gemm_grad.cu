@@ -7,8 +7,8 @@ namespace flce {
 namespace {
 
 template <int kCta, int kFp8>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                   const GemmParams& p, int grid, cudaStream_t stream) {
   auto kern = flce_gemm_kernel<EPI_GRAD, kCta, kFp8>;
   constexpr size_t smem = TileCfg<kCta>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -26,15 +26,19 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                           const GemmParams& p, int grid, cudaStream_t stream, int fp8) {
-  if (fp8) return cta_group == 2 ? launch<2, 1>(a, b, p, grid, stream) : launch<1, 1>(a, b, p, grid, stream);
-  return cta_group == 2 ? launch<2, 0>(a, b, p, grid, stream) : launch<1, 0>(a, b, p, grid, stream);
+                             const CUtensorMap& c, const GemmParams& p, int grid,
+                             cudaStream_t stream, int fp8) {
+  if (fp8)
+    return cta_group == 2 ? launch<2, 1>(a, b, c, p, grid, stream)
+                          : launch<1, 1>(a, b, c, p, grid, stream);
+  return cta_group == 2 ? launch<2, 0>(a, b, c, p, grid, stream)
+                        : launch<1, 0>(a, b, c, p, grid, stream);
 }
 
 }  // namespace flce

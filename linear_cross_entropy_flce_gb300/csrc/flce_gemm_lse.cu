@@ -26,7 +26,8 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, p);
+  const CUtensorMap unused = {};  // the LSE epilogue writes no tiles
+  return cudaLaunchKernelEx(&cfg, kern, a, b, unused, p);
 }
 
 }  // namespace

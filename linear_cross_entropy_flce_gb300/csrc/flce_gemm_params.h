@@ -36,13 +36,19 @@ struct TileCfg {
   static constexpr uint32_t kBBytes = kBRows * BK * 2;
   static constexpr uint32_t kSubBytes = kABytes + kBBytes;    // one K block, per CTA
   static constexpr uint32_t kStageBytes = kSub * kSubBytes;   // one ring stage, per CTA
-  static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  // Epilogue staging for TMA stores: two 4 KB boxes (32 rows x 128 bytes) per
+  // epilogue warp, after the ring.
+  static constexpr uint32_t kStgBytes = 4096;
+  static constexpr uint32_t kRingBytes = kStages * kStageBytes;
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + 4 * 2 * kStgBytes + 256;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum EpiKind { EPI_LSE = 0, EPI_GRAD = 1, EPI_F32 = 2 };
-enum OutMode { OUT_STORE_F32 = 0, OUT_ADD_F32 = 1, OUT_ADD_TO_BF16 = 2, OUT_STORE_BF16 = 3 };
+// Output of the fp32 epilogue through the output tensor map: store fp32, add fp32
+// to what is there (TMA reduce-add), or store rounded to bf16.
+enum OutMode { OUT_STORE_F32 = 0, OUT_ADD_F32 = 1, OUT_STORE_BF16 = 2 };
 
 constexpr int kStatusTimeout = 9;  // FLCE_ERR_TIMEOUT
 
@@ -93,16 +99,10 @@ struct GemmParams {
   float* zt;              // EPI_LSE: target logit per token
   const float* lse;       // EPI_GRAD: lse[row_base + row]
   const float* scale;     // EPI_GRAD: device scalar grad_scale / n
-  uint16_t* g_out;        // EPI_GRAD: G chunk, row stride g_ld elements
-  int64_t g_ld;
-  // EPI_F32
-  float* out_f32;
-  int64_t out_f32_ld;
-  int out_f32_row0;
-  uint16_t* out_bf16;
-  int64_t out_bf16_ld;
-  int out_bf16_row0;
-  int out_mode;
+  // EPI_GRAD and EPI_F32: the output map (third tensor map) holds product row r at
+  // map row out_row0 + r, product column c at map column c; boxes of 32 x 32.
+  int out_row0;
+  int out_mode;           // EPI_F32: OutMode (EPI_GRAD always stores bf16)
 };
 
 }  // namespace flce

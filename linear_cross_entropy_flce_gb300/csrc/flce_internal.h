@@ -13,12 +13,16 @@ namespace flce {
 
 // cta_group 1: grid CTAs of one; cta_group 2: grid/2 clusters of two CTAs.
 // fp8 = 1: E4M3 operands (kind::f8f6f4) scaled by p.acc_scale in the epilogue.
+// c is the output map of the epilogue's TMA stores (unused by the LSE epilogue):
+// bf16 G for the gradient GEMM; fp32 (or bf16 for OUT_STORE_BF16) for the F32 one.
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                             const GemmParams& p, int grid, cudaStream_t stream, int fp8);
+                             const CUtensorMap& c, const GemmParams& p, int grid,
+                             cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
-                            const GemmParams& p, int grid, cudaStream_t stream);
+                            const CUtensorMap& c, const GemmParams& p, int grid,
+                            cudaStream_t stream);
 
 // Per-token merge of the vocabulary-range partials into lse and the per-token
 // negative log-likelihood.
@@ -44,6 +48,10 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
                            int N, int V, int ignore_index, const float* scale, float* lse,
                            float* nll, void* g, int64_t gld_bytes, int sms,
                            cudaStream_t stream);
+
+// dst[i] = bf16(src[i]) (round to nearest even), n a multiple of 8, both 16-byte aligned.
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, int sms,
+                               cudaStream_t stream);
 
 // x (bf16 if bf16, else fp32; bytes a multiple of 16) *= *scale, in place.
 cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, int sms,

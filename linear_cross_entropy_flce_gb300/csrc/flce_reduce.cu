@@ -125,7 +125,37 @@ __global__ void scale_kernel(uint4* __restrict__ x, int64_t n16, const float* __
   }
 }
 
+// dst = bf16(src), round to nearest even, 8 elements (two 16-byte loads, one
+// 16-byte store) per thread and step: the last step of an fp32 accumulator that
+// the GEMM epilogue built by TMA reduce-adds (dH across vocabulary chunks, dW
+// across token blocks).
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                   int64_t n8) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = src[2 * i], b = src[2 * i + 1];
+    uint4 o;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(a.y), "f"(a.x));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(a.w), "f"(a.z));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(b.y), "f"(b.x));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(b.w), "f"(b.z));
+    dst[i] = o;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, int sms,
+                               cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  if (n8 <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (n8 + threads - 1) / threads;
+  const int grid = static_cast<int>(want < static_cast<int64_t>(sms) * 8 ? want : static_cast<int64_t>(sms) * 8);
+  f32_to_bf16_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                   reinterpret_cast<uint4*>(dst), n8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, int sms,
                          cudaStream_t stream) {
