@@ -686,6 +686,7 @@ int flce_ce_logits(const void* logits, int32_t dtype, int64_t ld, const int32_t*
     return FLCE_ERR_CUDA;
   if (flce::launch_ce_rows(dtype == FLCE_DTYPE_BF16 ? 1 : 0, logits, ld * elt, labels, Ni, Vi,
                            o.ignore_index, scal, lse ? lse : lse_ws, nll, dlogits, dld * elt, sms,
+                           status, o.timeout_ns > 0 ? o.timeout_ns : flce::kDefaultTimeoutNs,
                            st) != cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;

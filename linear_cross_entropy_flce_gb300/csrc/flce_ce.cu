@@ -8,13 +8,20 @@
 //
 // Kernels:
 //   ce_count_kernel : one block; n_valid, label check, gradient scale.
-//   ce_rows_kernel  : persistent clusters of 1-8 CTAs, one row per cluster at a
-//                     time, each CTA streaming a ~128 KB slice with 16-byte
-//                     vector loads; per-thread running (max, sum exp) merged
-//                     across the block and then across the cluster through
-//                     distributed shared memory; lse and the per-token loss, then
-//                     (optionally) the gradient of each slice, re-read from L2
-//                     (the live rows stay well inside the 129 MB L2).
+//   ce_rows_staged_kernel : rows of 64-768 KB. Persistent clusters of 1-8 CTAs,
+//                     one row per cluster at a time, each CTA's slice (at most
+//                     96 KB) copied into shared memory by the bulk-copy engine,
+//                     double-buffered so that the next row's slice streams in
+//                     while this one is reduced and its gradient written. Both
+//                     passes read shared memory: one DRAM read and one write per
+//                     element.
+//   ce_rows_kernel  : other rows. Persistent clusters of 1-8 CTAs, one row per
+//                     cluster at a time, each CTA streaming a ~128 KB slice with
+//                     16-byte vector loads; the gradient pass re-reads its slice
+//                     (from L2 when the live rows fit in it).
+// Both merge per-thread running (max, sum exp) across the block and then across
+// the cluster through distributed shared memory, then form lse and the
+// per-token loss.
 // The loss itself is formed by loss_reduce_kernel (flce_reduce.cu).
 #include <cmath>
 #include <cstdint>
@@ -246,6 +253,16 @@ __global__ void __launch_bounds__(kCeThreads)
       }
       if (lane == 0) s_part[it & 1] = make_float2(m, s);
     }
+    // The target logit is read before the cluster barrier: after it, peers may
+    // overwrite their slices with the gradient (in place).
+    int y = -1;
+    bool valid = false;
+    float zt = 0.f;
+    if (tid == 0) {
+      y = labels[row];
+      valid = y != ignore_index && y >= 0 && y < V;
+      if (crank == 0 && valid) zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
+    }
     // cluster merge through distributed shared memory
     cluster_barrier();
     if (tid == 0) {
@@ -255,10 +272,7 @@ __global__ void __launch_bounds__(kCeThreads)
         lse_merge(M, S, pr.x, pr.y);
       }
       const float lse = M + logf(S);
-      const int y = labels[row];
-      const bool valid = y != ignore_index && y >= 0 && y < V;
       if (crank == 0) {
-        const float zt = valid ? VT::load1(zr + static_cast<int64_t>(y) * kElt) : 0.f;
         if (lse_out != nullptr) lse_out[row] = lse;
         nll_out[row] = valid ? lse - zt : 0.f;
       }
@@ -300,6 +314,294 @@ __global__ void __launch_bounds__(kCeThreads)
   cluster_barrier();
 }
 
+// ---- shared-memory staged variant ---------------------------------------------
+
+constexpr int kStageSliceMax = 96 * 1024;  // bytes of one CTA's row slice (per buffer)
+constexpr int kBulkPiece = 16 * 1024;      // bytes per bulk copy instruction
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_phase_bounded(uint32_t bar, uint32_t parity,
+                                                   uint64_t timeout_ns) {
+  uint32_t done = 0;
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (i == 0) t0 = globaltimer_ns();
+    else if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// One row per cluster of CTAs; CTA r holds vectors [v0, v1) of every row it
+// visits in shared memory. Buffer (it & 1) receives row `it` of this cluster;
+// the copy of row it + 1 is issued before row it is reduced.
+template <int kBf16, bool kGrad>
+__global__ void __launch_bounds__(kCeThreads, 1)
+    ce_rows_staged_kernel(const uint8_t* z, int64_t ld_bytes,  // may alias g (in place)
+                          const int32_t* __restrict__ labels, int N, int V, int ignore_index,
+                          const float* __restrict__ scale_ptr, float* __restrict__ lse_out,
+                          float* __restrict__ nll_out, uint8_t* g, int64_t gld_bytes,
+                          int32_t* status, int64_t timeout_ns) {
+  using VT = Vec16<kBf16>;
+  constexpr int E = VT::E;
+  constexpr int kElt = kBf16 ? 2 : 4;
+  extern __shared__ __align__(128) uint8_t ce_smem[];
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ float2 s_red[kCeThreads / 32];
+  __shared__ float2 s_part[2];
+  __shared__ float s_lse;
+  __shared__ int s_y;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const float scale = kGrad ? *scale_ptr : 0.f;
+  const int nvec = V / E;
+  const int crank = static_cast<int>(cta_rank_in_cluster());
+  const int csize = static_cast<int>(ctas_in_cluster());
+  const int cluster = static_cast<int>(blockIdx.x) / csize;
+  const int nclusters = static_cast<int>(gridDim.x) / csize;
+  const int per = (nvec + csize - 1) / csize;
+  const int v0 = min(nvec, crank * per), v1 = min(nvec, v0 + per);
+  const int nv = v1 - v0;                      // vectors in this CTA's slice
+  const uint32_t slice_bytes = static_cast<uint32_t>(nv) * 16u;
+  const bool last = crank == csize - 1;
+  uint8_t* buf[2] = {ce_smem, ce_smem + kStageSliceMax};
+  const uint32_t bar0 = smem_addr(&s_bar[0]), bar1 = smem_addr(&s_bar[1]);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // thread 0: expect the slice's bytes on the buffer's barrier and copy it
+  auto issue = [&](int row, int b) {
+    const uint32_t bar = b ? bar1 : bar0;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(slice_bytes)
+                 : "memory");
+    const uint8_t* src = z + static_cast<int64_t>(row) * ld_bytes + static_cast<int64_t>(v0) * 16;
+    const uint32_t dst = smem_addr(buf[b]);
+    for (uint32_t off = 0; off < slice_bytes; off += kBulkPiece) {
+      const uint32_t n = min(static_cast<uint32_t>(kBulkPiece), slice_bytes - off);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              dst + off),
+          "l"(src + off), "r"(n), "r"(bar)
+          : "memory");
+    }
+  };
+
+  int it = 0;
+  int row = cluster;
+  if (tid == 0 && row < N && nv > 0) issue(row, 0);
+  bool timed_out = false;
+  for (; row < N; row += nclusters, ++it) {
+    const int b = it & 1;
+    const uint8_t* zr = z + static_cast<int64_t>(row) * ld_bytes;
+    // the next row's slice streams into the other buffer meanwhile (its last
+    // reader, the previous row, finished at the end of the previous iteration)
+    if (tid == 0 && row + nclusters < N && nv > 0) issue(row + nclusters, b ^ 1);
+    if (nv > 0 && !wait_phase_bounded(b ? bar1 : bar0, static_cast<uint32_t>((it >> 1) & 1),
+                                      static_cast<uint64_t>(timeout_ns)))
+      timed_out = true;
+    const uint8_t* sl = buf[b];
+    // pass 1: running max and sum of exponentials over the staged slice
+    float m = -INFINITY, s = 0.f;
+    {
+      constexpr int kU = 2;
+      int v = tid;
+      for (; v + (kU - 1) * kCeThreads < nv; v += kU * kCeThreads) {
+        float x[kU][E];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v + u * kCeThreads) * 16);
+          if constexpr (kBf16) {
+            x[u][0] = bf16_lo(w.x); x[u][1] = bf16_hi(w.x); x[u][2] = bf16_lo(w.y); x[u][3] = bf16_hi(w.y);
+            x[u][4] = bf16_lo(w.z); x[u][5] = bf16_hi(w.z); x[u][6] = bf16_lo(w.w); x[u][7] = bf16_hi(w.w);
+          } else {
+            x[u][0] = __uint_as_float(w.x); x[u][1] = __uint_as_float(w.y);
+            x[u][2] = __uint_as_float(w.z); x[u][3] = __uint_as_float(w.w);
+          }
+        }
+        float cm = m;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[u][e]);
+        const float ms = cm * kLog2e;
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc += ex2a(fmaf(x[u][e], kLog2e, -ms));
+        if (cm != -INFINITY) {
+          s = s * ex2a((m - cm) * kLog2e) + acc;
+          m = cm;
+        }
+      }
+      for (; v < nv; v += kCeThreads) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+        float x[E];
+        if constexpr (kBf16) {
+          x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+          x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+        } else {
+          x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+          x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+        }
+        float cm = m;
+#pragma unroll
+        for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[e]);
+        if (cm == -INFINITY) continue;
+        const float ms = cm * kLog2e;
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc += ex2a(fmaf(x[e], kLog2e, -ms));
+        s = s * ex2a((m - cm) * kLog2e) + acc;
+        m = cm;
+      }
+    }
+    if (last) {
+      for (int i = nvec * E + tid; i < V; i += kCeThreads) {
+        const float x = VT::load1(zr + static_cast<int64_t>(i) * kElt);
+        lse_merge(m, s, x, 1.f);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    if (lane == 0) s_red[warp] = make_float2(m, s);
+    __syncthreads();
+    if (warp == 0) {
+      float2 r = lane < kCeThreads / 32 ? s_red[lane] : make_float2(-INFINITY, 0.f);
+      m = r.x;
+      s = r.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        lse_merge(m, s, m2, s2);
+      }
+      if (lane == 0) s_part[it & 1] = make_float2(m, s);
+    }
+    // The target logit is read before the cluster barrier: after it, peers may
+    // overwrite their slices with the gradient (in place).
+    int y = -1;
+    bool valid = false;
+    float zt = 0.f;
+    if (tid == 0) {
+      y = labels[row];
+      valid = y != ignore_index && y >= 0 && y < V;
+      if (crank == 0 && valid) zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
+    }
+    cluster_barrier();
+    if (tid == 0) {
+      float M = -INFINITY, S = 0.f;
+      for (int r = 0; r < csize; ++r) {
+        const float2 pr = ld_dsmem_f2(&s_part[it & 1], static_cast<uint32_t>(r));
+        lse_merge(M, S, pr.x, pr.y);
+      }
+      const float lse = M + logf(S);
+      if (crank == 0) {
+        if (lse_out != nullptr) lse_out[row] = lse;
+        nll_out[row] = valid ? lse - zt : 0.f;
+      }
+      s_lse = lse;
+      s_y = valid ? y : -1;
+    }
+    __syncthreads();
+    if constexpr (kGrad) {
+      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale from the staged slice
+      const float lse = s_lse;
+      const int y = s_y;
+      const float sc = y >= 0 ? scale : 0.f;
+      const float nl2 = -lse * kLog2e;
+      uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
+      for (int v = tid; v < nv; v += kCeThreads) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+        float x[E];
+        if constexpr (kBf16) {
+          x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+          x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+        } else {
+          x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+          x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
+        const int base = (v0 + v) * E;
+        if (static_cast<unsigned>(y - base) < static_cast<unsigned>(E)) {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (base + e == y) x[e] -= sc;
+        }
+        VT::store(gr + static_cast<int64_t>(v0 + v) * 16, x);
+      }
+      if (last) {
+        for (int i = nvec * E + tid; i < V; i += kCeThreads) {
+          float x = ex2a(fmaf(VT::load1(zr + static_cast<int64_t>(i) * kElt), kLog2e, nl2)) * sc;
+          if (i == y) x -= sc;
+          VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
+        }
+      }
+    }
+    __syncthreads();  // the buffer, s_red, s_lse, s_y are reused
+  }
+  if (timed_out && status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, 9);
+  cluster_barrier();
+}
+
+template <int kBf16, bool kGrad>
+cudaError_t launch_rows_staged(int cluster, int grid, const uint8_t* z, int64_t ld_bytes,
+                               const int32_t* labels, int N, int V, int ignore_index,
+                               const float* scale, float* lse, float* nll, uint8_t* g,
+                               int64_t gld_bytes, int32_t* status, int64_t timeout_ns,
+                               cudaStream_t stream) {
+  auto kern = ce_rows_staged_kernel<kBf16, kGrad>;
+  constexpr int smem = 2 * kStageSliceMax;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kCeThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent clusters: launch only as many as can be resident at once (a
+  // cluster that had to wait for a free GPC would run its rows after the rest)
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0 &&
+      active * cluster < grid)
+    cfg.gridDim = dim3(static_cast<unsigned>(active * cluster), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, z, ld_bytes, labels, N, V, ignore_index, scale, lse, nll,
+                            g, gld_bytes, status, timeout_ns);
+}
+
 template <int kBf16, bool kGrad>
 cudaError_t launch_rows(int cluster, int grid, const uint8_t* z, int64_t ld_bytes,
                         const int32_t* labels, int N, int V, int ignore_index, const float* scale,
@@ -333,8 +635,35 @@ cudaError_t launch_ce_count(const int32_t* labels, int N, int V, int ignore_inde
 
 cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int32_t* labels,
                            int N, int V, int ignore_index, const float* scale, float* lse,
-                           float* nll, void* g, int64_t gld_bytes, int sms,
-                           cudaStream_t stream) {
+                           float* nll, void* g, int64_t gld_bytes, int sms, int32_t* status,
+                           int64_t timeout_ns, cudaStream_t stream) {
+  // Rows of 64-768 KB: slices of at most 96 KB staged in shared memory by a
+  // cluster of ceil(row / 96 KB) CTAs, one CTA per SM.
+  const int64_t vec_bytes = static_cast<int64_t>(V / (bf16 ? 8 : 4)) * 16;
+  if (vec_bytes >= (64 << 10) && vec_bytes <= 8 * static_cast<int64_t>(kStageSliceMax)) {
+    int cl = static_cast<int>((vec_bytes + kStageSliceMax - 1) / kStageSliceMax);
+    // the slices are whole 16-byte vectors: make sure the rounding up of the
+    // per-CTA vector count keeps every slice within one buffer
+    while (cl < 8 && ((vec_bytes / 16 + cl - 1) / cl) * 16 > kStageSliceMax) ++cl;
+    int ncl = sms / cl;
+    if (ncl > N) ncl = N;
+    if (ncl < 1) ncl = 1;
+    const uint8_t* zp = static_cast<const uint8_t*>(z);
+    uint8_t* gp = static_cast<uint8_t*>(g);
+    if (bf16)
+      return g ? launch_rows_staged<1, true>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
+                                             ignore_index, scale, lse, nll, gp, gld_bytes,
+                                             status, timeout_ns, stream)
+               : launch_rows_staged<1, false>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
+                                              ignore_index, scale, lse, nll, gp, gld_bytes,
+                                              status, timeout_ns, stream);
+    return g ? launch_rows_staged<0, true>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
+                                           ignore_index, scale, lse, nll, gp, gld_bytes, status,
+                                           timeout_ns, stream)
+             : launch_rows_staged<0, false>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
+                                            ignore_index, scale, lse, nll, gp, gld_bytes, status,
+                                            timeout_ns, stream);
+  }
   // Cluster size: slices of about 256 KB of a row per CTA, at least two CTAs for
   // rows over 128 KB, at most eight; two CTAs per SM (the register budget of a
   // 512-thread CTA), rounded down to whole clusters, no more clusters than rows.

@@ -46,8 +46,8 @@ cudaError_t launch_ce_count(const int32_t* labels, int N, int V, int ignore_inde
                             cudaStream_t stream);
 cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int32_t* labels,
                            int N, int V, int ignore_index, const float* scale, float* lse,
-                           float* nll, void* g, int64_t gld_bytes, int sms,
-                           cudaStream_t stream);
+                           float* nll, void* g, int64_t gld_bytes, int sms, int32_t* status,
+                           int64_t timeout_ns, cudaStream_t stream);
 
 // dst[i] = bf16(src[i]) (round to nearest even), n a multiple of 8, both 16-byte aligned.
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, int sms,

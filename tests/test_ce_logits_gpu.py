@@ -126,3 +126,35 @@ def test_matches_fused_loss_on_the_same_logits():
     torch.cuda.synchronize()
     assert abs(float(ce.loss.item()) - float(fu.loss.item())) <= 1e-4 * float(fu.loss.item())
     assert float((ce.lse - fu.lse).abs().max()) <= 1e-3
+
+
+@pytest.mark.parametrize("N,V,bf16", [
+    (40, 128256, False),   # 501 KB rows: staged slices, cluster of 6
+    (24, 128257, True),    # 250 KB bf16 rows with a scalar tail: staged, cluster of 3
+    (9, 100003, False),    # staged, ragged fp32 tail
+    (5, 200003, False),    # 781 KB rows: streamed kernel, cluster of 4
+])
+def test_long_rows_parity_and_in_place(N, V, bf16):
+    """Rows long enough for multi-CTA clusters (shared-memory staged slices, or
+    the streamed kernel past 768 KB): parity with the oracle, and the in-place
+    gradient bitwise equal to the out-of-place one (the target logit must be read
+    before any CTA of the cluster overwrites its slice)."""
+    ld = (V + 7) // 8 * 8
+    Z, y, t, lab = _logits(N, V, seed=N + V % 997, bf16=bf16, ld=ld)
+
+    def padded_clone(x):  # same padded row stride (16-byte aligned rows)
+        full = torch.zeros(N, ld, dtype=x.dtype, device=x.device)
+        full[:, :V].copy_(x)
+        return full[:, :V]
+
+    a = flce.ce_logits(padded_clone(t), lab)
+    assert flce.check_status(a.status) == flce.FLCE_OK
+    _check(a, oracle.ce_logits(Z, y))
+    tc = padded_clone(t)
+    b = flce.ce_logits(tc, lab, in_place=True)
+    torch.cuda.synchronize()
+    assert flce.check_status(b.status) == flce.FLCE_OK
+    assert b.dlogits.data_ptr() == tc.data_ptr()
+    assert torch.equal(a.dlogits.view(torch.int16 if bf16 else torch.int32),
+                       b.dlogits.view(torch.int16 if bf16 else torch.int32))
+    assert torch.equal(a.loss, b.loss) and torch.equal(a.lse, b.lse)
