@@ -21,9 +21,10 @@
 //   warp 0     : TMA producer (one thread per CTA) — streams the CTA's A rows and
 //                B half, K-slice by K-slice, into a ring of shared-memory stages;
 //                the copies of both CTAs complete on the even CTA's stage barrier.
-//   warp 1     : TMEM allocator (both CTAs) and MMA issuer (one thread of the even
-//                CTA) — tcgen05.mma M x 256 x 16 steps into one of two TMEM
-//                accumulators.
+//   warp 1     : TMEM allocator (both CTAs) and MMA issuer (the even CTA's warp:
+//                all lanes wait on the barriers, one elected lane issues the
+//                tcgen05.mma M x 256 x 16 steps into one of two TMEM accumulators
+//                and the commits).
 //   warps 2..5 : epilogue — warp w reads TMEM lanes 32*(w%4) .. +31, so each
 //                thread owns one output row of its CTA's 128 rows.
 // Every wait is bounded (see mbar_wait_bounded); on a timeout the CTA records
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (even CTA) ----------------
-    if (lane == 0 && leader) {
+    if (leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -343,19 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             got = mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, tmo, abort_flag);
           }
-          if (!got) {
+          if (!__all_sync(0xffffffffu, got)) {  // one decision for the whole warp
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int ks = 0; ks < k_stages; ++ks) {
-            if (!mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag)) {
+            const bool full_ok = mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag);
+            if (!__all_sync(0xffffffffu, full_ok)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const int nsub = min(kSub, p.k_blocks - ks * kSub);
+            if (elect_one()) {
 #pragma unroll
             for (int sub = 0; sub < kSub; ++sub) {
               if (sub >= nsub) break;
@@ -372,15 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, accum);
               }
             }
-            issued_any = true;
             umma_commit_pair<kCta>(empty_bar(stage));  // frees the stage in both CTAs
+            }
+            __syncwarp();
+            issued_any = true;
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit_pair<kCta>(tfull_bar(acc));
+          if (elect_one()) umma_commit_pair<kCta>(tfull_bar(acc));
+          __syncwarp();
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -388,13 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        record_status(p.status, kStatusTimeout);
+        if (lane == 0) record_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
       if (issued_any) {
-        // Drain: all MMAs of this thread complete before TMEM is freed.
+        // Drain: all MMAs of this warp complete before TMEM is freed.
         const volatile int no_abort = 0;
-        umma_commit_cg<kCta>(drain_bar);
+        if (lane == 0) umma_commit_cg<kCta>(drain_bar);
+        __syncwarp();
         mbar_wait_bounded(drain_bar, 0, 1000000000ull, &no_abort);
       }
     }
