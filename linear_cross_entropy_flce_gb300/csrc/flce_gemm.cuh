@@ -18,9 +18,10 @@
 // 128 x 256 tile. kCta = 2: a cluster pair computes a 256 x 256 tile with
 // tcgen05 cta_group::2 MMAs; each CTA holds its 128 rows of A and 128 of the 256
 // rows of B, and its own 128 x 256 fp32 accumulator rows in TMEM.
-//   warp 0     : TMA producer (one thread per CTA) — streams the CTA's A rows and
-//                B half, K-slice by K-slice, into a ring of shared-memory stages;
-//                the copies of both CTAs complete on the even CTA's stage barrier.
+//   warp 0     : TMA producer (each CTA; all lanes wait, one elected lane issues)
+//                — streams the CTA's A rows and B half, K-slice by K-slice, into a
+//                ring of shared-memory stages; the copies of both CTAs complete on
+//                the even CTA's stage barrier.
 //   warp 1     : TMEM allocator (both CTAs) and MMA issuer (the even CTA's warp:
 //                all lanes wait on the barriers, one elected lane issues the
 //                tcgen05.mma M x 256 x 16 steps into one of two TMEM accumulators
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (each CTA loads its own A rows and B half) -----
-    if (lane == 0) {
+    {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
@@ -241,10 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
           for (int ks = 0; ks < k_stages; ++ks) {
-            if (!mbar_wait_bounded<kCl>(empty_bar(stage), phase ^ 1u, tmo, abort_flag)) {
+            const bool empty_ok = mbar_wait_bounded<kCl>(empty_bar(stage), phase ^ 1u, tmo, abort_flag);
+            if (!__all_sync(0xffffffffu, empty_ok)) {  // one decision for the whole warp
               ok = false;
               break;
             }
+            if (elect_one()) {
             const int nsub = min(kSub, p.k_blocks - ks * kSub);
             const uint32_t fb_local = full_bar(stage);
             if (leader)
@@ -286,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
               }
             }
+            }
+            __syncwarp();
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        record_status(p.status, kStatusTimeout);
+        if (lane == 0) record_status(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
       // Drain before the final barrier. The even CTA waits for every stage phase it
