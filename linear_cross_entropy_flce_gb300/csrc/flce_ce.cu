@@ -316,7 +316,11 @@ __global__ void __launch_bounds__(kCeThreads)
 
 // ---- shared-memory staged variant ---------------------------------------------
 
-constexpr int kStageSliceMax = 96 * 1024;  // bytes of one CTA's row slice (per buffer)
+// Slices of at most 96 KB with one CTA per SM, or (bf16 rows, whose passes carry
+// twice the exponentials per byte) at most 56 KB with two CTAs per SM, so that
+// one CTA's reduction overlaps the other's gradient writes.
+constexpr int kSliceOne = 96 * 1024;
+constexpr int kSliceTwo = 56 * 1024;
 constexpr int kBulkPiece = 16 * 1024;      // bytes per bulk copy instruction
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -350,8 +354,8 @@ __device__ __forceinline__ bool wait_phase_bounded(uint32_t bar, uint32_t parity
 // One row per cluster of CTAs; CTA r holds vectors [v0, v1) of every row it
 // visits in shared memory. Buffer (it & 1) receives row `it` of this cluster;
 // the copy of row it + 1 is issued before row it is reduced.
-template <int kBf16, bool kGrad>
-__global__ void __launch_bounds__(kCeThreads, 1)
+template <int kBf16, bool kGrad, int kSlice, int kMinB>
+__global__ void __launch_bounds__(kCeThreads, kMinB)
     ce_rows_staged_kernel(const uint8_t* z, int64_t ld_bytes,  // may alias g (in place)
                           const int32_t* __restrict__ labels, int N, int V, int ignore_index,
                           const float* __restrict__ scale_ptr, float* __restrict__ lse_out,
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kCeThreads, 1)
   const int nv = v1 - v0;                      // vectors in this CTA's slice
   const uint32_t slice_bytes = static_cast<uint32_t>(nv) * 16u;
   const bool last = crank == csize - 1;
-  uint8_t* buf[2] = {ce_smem, ce_smem + kStageSliceMax};
+  uint8_t* buf[2] = {ce_smem, ce_smem + kSlice};
   const uint32_t bar0 = smem_addr(&s_bar[0]), bar1 = smem_addr(&s_bar[1]);
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
@@ -570,14 +574,14 @@ __global__ void __launch_bounds__(kCeThreads, 1)
   cluster_barrier();
 }
 
-template <int kBf16, bool kGrad>
+template <int kBf16, bool kGrad, int kSlice, int kMinB>
 cudaError_t launch_rows_staged(int cluster, int grid, const uint8_t* z, int64_t ld_bytes,
                                const int32_t* labels, int N, int V, int ignore_index,
                                const float* scale, float* lse, float* nll, uint8_t* g,
                                int64_t gld_bytes, int32_t* status, int64_t timeout_ns,
                                cudaStream_t stream) {
-  auto kern = ce_rows_staged_kernel<kBf16, kGrad>;
-  constexpr int smem = 2 * kStageSliceMax;
+  auto kern = ce_rows_staged_kernel<kBf16, kGrad, kSlice, kMinB>;
+  constexpr int smem = 2 * kSlice;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -637,32 +641,48 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
                            int N, int V, int ignore_index, const float* scale, float* lse,
                            float* nll, void* g, int64_t gld_bytes, int sms, int32_t* status,
                            int64_t timeout_ns, cudaStream_t stream) {
-  // Rows of 64-768 KB: slices of at most 96 KB staged in shared memory by a
-  // cluster of ceil(row / 96 KB) CTAs, one CTA per SM.
+  // Rows of 64-768 KB: slices staged in shared memory by a cluster of
+  // ceil(row / slice) CTAs (at most eight).
   const int64_t vec_bytes = static_cast<int64_t>(V / (bf16 ? 8 : 4)) * 16;
-  if (vec_bytes >= (64 << 10) && vec_bytes <= 8 * static_cast<int64_t>(kStageSliceMax)) {
-    int cl = static_cast<int>((vec_bytes + kStageSliceMax - 1) / kStageSliceMax);
+  auto cluster_for = [&](int64_t slice) -> int {
+    if (vec_bytes < (64 << 10) || vec_bytes > 8 * slice) return 0;
+    int cl = static_cast<int>((vec_bytes + slice - 1) / slice);
     // the slices are whole 16-byte vectors: make sure the rounding up of the
     // per-CTA vector count keeps every slice within one buffer
-    while (cl < 8 && ((vec_bytes / 16 + cl - 1) / cl) * 16 > kStageSliceMax) ++cl;
-    int ncl = sms / cl;
+    while (cl < 8 && ((vec_bytes / 16 + cl - 1) / cl) * 16 > slice) ++cl;
+    return ((vec_bytes / 16 + cl - 1) / cl) * 16 <= slice ? cl : 0;
+  };
+  const uint8_t* zp = static_cast<const uint8_t*>(z);
+  uint8_t* gp = static_cast<uint8_t*>(g);
+  auto clusters = [&](int cl, int per_sm) {
+    int ncl = per_sm * sms / cl;
     if (ncl > N) ncl = N;
-    if (ncl < 1) ncl = 1;
-    const uint8_t* zp = static_cast<const uint8_t*>(z);
-    uint8_t* gp = static_cast<uint8_t*>(g);
+    return ncl < 1 ? 1 : ncl;
+  };
+  if (int cl = bf16 ? cluster_for(kSliceTwo) : 0) {
+    const int grid = clusters(cl, 2) * cl;
+    return g ? launch_rows_staged<1, true, kSliceTwo, 2>(cl, grid, zp, ld_bytes, labels, N, V,
+                                                         ignore_index, scale, lse, nll, gp,
+                                                         gld_bytes, status, timeout_ns, stream)
+             : launch_rows_staged<1, false, kSliceTwo, 2>(cl, grid, zp, ld_bytes, labels, N, V,
+                                                          ignore_index, scale, lse, nll, gp,
+                                                          gld_bytes, status, timeout_ns, stream);
+  }
+  if (int cl = cluster_for(kSliceOne)) {
+    const int grid = clusters(cl, 1) * cl;
     if (bf16)
-      return g ? launch_rows_staged<1, true>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
-                                             ignore_index, scale, lse, nll, gp, gld_bytes,
-                                             status, timeout_ns, stream)
-               : launch_rows_staged<1, false>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
-                                              ignore_index, scale, lse, nll, gp, gld_bytes,
-                                              status, timeout_ns, stream);
-    return g ? launch_rows_staged<0, true>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
-                                           ignore_index, scale, lse, nll, gp, gld_bytes, status,
-                                           timeout_ns, stream)
-             : launch_rows_staged<0, false>(cl, ncl * cl, zp, ld_bytes, labels, N, V,
-                                            ignore_index, scale, lse, nll, gp, gld_bytes, status,
-                                            timeout_ns, stream);
+      return g ? launch_rows_staged<1, true, kSliceOne, 1>(cl, grid, zp, ld_bytes, labels, N, V,
+                                                           ignore_index, scale, lse, nll, gp,
+                                                           gld_bytes, status, timeout_ns, stream)
+               : launch_rows_staged<1, false, kSliceOne, 1>(cl, grid, zp, ld_bytes, labels, N,
+                                                            V, ignore_index, scale, lse, nll, gp,
+                                                            gld_bytes, status, timeout_ns, stream);
+    return g ? launch_rows_staged<0, true, kSliceOne, 1>(cl, grid, zp, ld_bytes, labels, N, V,
+                                                         ignore_index, scale, lse, nll, gp,
+                                                         gld_bytes, status, timeout_ns, stream)
+             : launch_rows_staged<0, false, kSliceOne, 1>(cl, grid, zp, ld_bytes, labels, N, V,
+                                                          ignore_index, scale, lse, nll, gp,
+                                                          gld_bytes, status, timeout_ns, stream);
   }
   // Cluster size: slices of about 256 KB of a row per CTA, at least two CTAs for
   // rows over 128 KB, at most eight; two CTAs per SM (the register budget of a
@@ -673,12 +693,7 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
   int cluster = static_cast<int>((row_bytes + (256 << 10) - 1) / (256 << 10));
   if (row_bytes > (128 << 10) && cluster < 2) cluster = 2;
   cluster = cluster < 1 ? 1 : (cluster > 8 ? 8 : cluster);
-  int clusters = (2 * sms) / cluster;
-  if (clusters > N) clusters = N;
-  if (clusters < 1) clusters = 1;
-  const int grid = clusters * cluster;
-  const uint8_t* zp = static_cast<const uint8_t*>(z);
-  uint8_t* gp = static_cast<uint8_t*>(g);
+  const int grid = clusters(cluster, 2) * cluster;
   cudaError_t e;
   if (bf16) {
     e = g ? launch_rows<1, true>(cluster, grid, zp, ld_bytes, labels, N, V, ignore_index, scale,
