@@ -543,7 +543,8 @@ def main(argv=None) -> int:
                 flce.forward_backward(Hd, Wd, yd, out=out, workspace=ws, status=status,
                                       stream=stream.cuda_stream, **plan_kw)
                 consumed[b].record(stream)
-                loss_host[slot0 + i:slot0 + i + 1].copy_(out["loss"], non_blocking=True)
+                with torch.cuda.stream(stream):  # ordered after this step's kernels
+                    loss_host[slot0 + i:slot0 + i + 1].copy_(out["loss"], non_blocking=True)
 
         run_e2e(args.warmup, 0)
         torch.cuda.synchronize(dev)
