@@ -212,7 +212,7 @@ def run_reference(args, wl, world, rank):
     """The reference arm: the float64 CPU oracle, each step a bounded sample."""
     if rank != 0:
         return 0
-    tokens = args.ref_tokens
+    tokens = min(args.ref_tokens, wl.N)  # a sample of the workload, never more
     for _ in range(args.warmup):
         cpu_oracle_sample(wl, tokens)
     times = [cpu_oracle_sample(wl, tokens)["seconds"] for _ in range(args.steps)]
@@ -604,7 +604,7 @@ def main(argv=None) -> int:
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        r = cpu_oracle_sample(wl, args.cpu_tokens)
+        r = cpu_oracle_sample(wl, min(args.cpu_tokens, wl.N))
         cpu = {"value": r["tokens"] / r["seconds"], "unit": UNIT, "cores": blas_threads(),
                "kind": "oracle", "seconds": r["seconds"],
                "sample": f"first {r['tokens']} tokens of the {wl.name} workload, full V={V} "
