@@ -92,3 +92,32 @@ def test_shift_of_every_weight_row_changes_only_lse():
     assert np.max(np.abs(dl - hc)) <= 2e-3
     assert rel_fro(tensor_to_f64(b.dH), tensor_to_f64(a.dH)) <= 5e-3
     assert rel_fro(tensor_to_f64(b.dW), tensor_to_f64(a.dW)) <= 5e-3
+
+
+@pytest.mark.parametrize("N,V,bf16", [(40, 128256, False), (24, 128257, True), (5, 200003, False),
+                                      (33, 5003, False)])
+def test_ce_logits_writes_only_the_gradient_rows(N, V, bf16):
+    """Cross-entropy over given logits with a padded gradient buffer: the row
+    padding and the guard bytes around the gradient, lse and loss keep their
+    pattern (staged and streamed row kernels)."""
+    dev = torch.device("cuda:0")
+    esz = 2 if bf16 else 4
+    ld = (V + 15) // 16 * 16
+    g = np.random.Generator(np.random.Philox(np.random.SeedSequence([V, N])))
+    Z = torch.from_numpy((g.standard_normal((N, V), dtype=np.float32) * 1.3)).to(dev)
+    Z = Z.to(torch.bfloat16) if bf16 else Z
+    zfull = torch.zeros(N, ld, dtype=Z.dtype, device=dev)
+    zfull[:, :V] = Z
+    lab = torch.from_numpy(g.integers(0, V, N).astype(np.int32)).to(dev)
+    gbuf, graw = _guarded(N * ld * esz, dev)
+    gview = graw.view(torch.bfloat16 if bf16 else torch.float32).view(N, ld)[:, :V]
+    lbuf, lraw = _guarded(N * 4, dev)
+    sbuf, sraw = _guarded(4, dev)
+    res = flce.ce_logits(zfull[:, :V], lab, out={"dlogits": gview, "lse": lraw.view(torch.float32),
+                                                 "loss": sraw.view(torch.float32)})
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    for name, b in (("dlogits", gbuf), ("lse", lbuf), ("loss", sbuf)):
+        assert _guards_intact(b), name
+    pad = graw.view(N, ld * esz)[:, V * esz:].cpu().numpy()
+    assert (pad == PATTERN).all()
+    assert torch.isfinite(res.dlogits.float()).all()
