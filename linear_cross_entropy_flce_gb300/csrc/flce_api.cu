@@ -118,6 +118,29 @@ bool encode_out(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint
   return r == CUDA_SUCCESS;
 }
 
+// The bf16 G chunk is stored chunk-major, [v_chunk/64][rows][64]: the 64 vocabulary
+// ids of one K block of the dH product, or one 64-wide MN chunk of the dW product,
+// are contiguous for a run of rows, so each copy of a consumer reads whole
+// contiguous blocks (8-16 KB) instead of 128-byte pieces of rows v_chunk·2 bytes
+// apart. Three views of it: the gradient epilogue's 32 x 32 store boxes, the
+// K-major A operand of dH (64 ids x 128 rows per box) and the MN-major A operand of
+// dW (64 ids x 64 rows x 2 chunks per box).
+bool encode_g_chunked(CUtensorMap* m, void* G, uint64_t rows, uint64_t v_chunk, uint32_t box_x,
+                      uint32_t box_y, uint32_t box_z, bool sw64) {
+  auto fn = encode_fn();
+  if (fn == nullptr || v_chunk % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, v_chunk / 64};
+  cuuint64_t strides[2] = {128, rows * 128};
+  cuuint32_t box[3] = {box_x, box_y, box_z};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, G, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  sw64 ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tiles are computed by cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int kCtaGroup = 2;
 
@@ -416,9 +439,9 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
                            : encode_bf16(&mH_mn, H, D, N, D, 64, BK);
   const bool ok_w = d_box3 ? encode_bf16_mn3(&mW_mn, W, D, V, D, BK, b_chunks)
                            : encode_bf16(&mW_mn, W, D, V, D, 64, BK);
-  if (!ok_h || !ok_w || !encode_bf16_mn3(&mG_mn, G, P.v_chunk, rows_b, P.v_chunk, BK, BM / 64) ||
-      !encode_bf16(&mG_k, G, P.v_chunk, rows_b, P.v_chunk, BK, BM) ||
-      !encode_out(&mG_out, G, true, P.v_chunk, rows_b, P.v_chunk))
+  if (!ok_h || !ok_w || !encode_g_chunked(&mG_mn, G, rows_b, P.v_chunk, 64, BK, BM / 64, false) ||
+      !encode_g_chunked(&mG_k, G, rows_b, P.v_chunk, 64, BM, 1, false) ||
+      !encode_g_chunked(&mG_out, G, rows_b, P.v_chunk, 32, 32, 1, true))
     return FLCE_ERR_CUDA;
   const bool dw_bf16 = o.dw_dtype == FLCE_DTYPE_BF16;
   // dW goes to fp32 dW, to bf16 dW (one token block), or to the fp32 accumulator
@@ -499,6 +522,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         // dH rows [b0, b0 + nb_len) (+)= G_bc W_c: M = tokens, N = hidden, K = vocabulary.
         GemmParams h{};
         h.a_mn_major = 0;
+        h.a_kchunk = 1;
         h.b_mn_major = 1;
         h.b_box3 = d_box3 ? 1 : 0;
         h.b_k0 = static_cast<int>(c0);

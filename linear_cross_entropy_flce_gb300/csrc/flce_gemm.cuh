@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int kx = (ks * kSub + sub) * (kFp8 ? 2 * BK : BK);  // elements per 128-byte row
               const uint32_t sa = stage0 + stage * Cfg::kStageBytes + sub * Cfg::kSubBytes;
               const uint32_t sb = sa + Cfg::kABytes;
-              if (!p.a_mn_major) {
+              if (!p.a_mn_major && p.a_kchunk) {
+                load3(sa, &tmA, am + p.a_mn0, (kx + p.a_k0) >> 6, pol_a);
+              } else if (!p.a_mn_major) {
                 load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
               } else if (p.a_box3) {
                 load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
@@ -505,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // rows and columns outside the map are dropped by the store
               const int oy = p.out_row0 + m_blk * Cfg::kTileM + static_cast<int>(rank) * BM +
                              quarter * 32;
-              if (kEpi == EPI_F32 && p.out_mode == OUT_ADD_F32) tma_reduce_add_2d(&tmC, box, col, oy);
+              if constexpr (kEpi == EPI_GRAD) tma_store_3d(&tmC, box, col & 63, oy, col >> 6);
+              else if (p.out_mode == OUT_ADD_F32) tma_reduce_add_2d(&tmC, box, col, oy);
               else tma_store_2d(&tmC, box, col, oy);
               bulk_commit_group();
             }

@@ -76,6 +76,9 @@ struct GemmParams {
   // MN-major operand given as a 3-D map [MN/64][K][64] (MN extent a multiple of 64):
   // one copy per CTA fills all of its 64-wide chunks; coordinate z = mn / 64.
   int a_box3, b_box3;
+  // K-major A stored chunk-major, [K/64][rows][64] (the G chunk): one 3-D copy with
+  // coordinates (0, row, k / 64) per K block.
+  int a_kchunk;
   int a_mn0, a_k0, b_mn0, b_k0;
   int m_blocks, n_blocks, k_blocks;  // m_blocks counts tiles of TileCfg::kTileM rows
   int num_units;
@@ -99,8 +102,9 @@ struct GemmParams {
   float* zt;              // EPI_LSE: target logit per token
   const float* lse;       // EPI_GRAD: lse[row_base + row]
   const float* scale;     // EPI_GRAD: device scalar grad_scale / n
-  // EPI_GRAD and EPI_F32: the output map (third tensor map) holds product row r at
-  // map row out_row0 + r, product column c at map column c; boxes of 32 x 32.
+  // EPI_F32: the output map (third tensor map) holds product row r at map row
+  // out_row0 + r, product column c at map column c; boxes of 32 x 32. EPI_GRAD: the
+  // map is the chunk-major G, [columns/64][rows][64], boxes of 32 x 32 x 1.
   int out_row0;
   int out_mode;           // EPI_F32: OutMode (EPI_GRAD always stores bf16)
 };

@@ -391,6 +391,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sm
       : "memory");
 }
 
+// 3-D tiled bulk tensor store (x innermost).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t smem_src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_src)
+      : "memory");
+}
+
 // As tma_store_2d, but each element is added to the global value (fp32 add,
 // performed by the memory system; one add per element per call).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t smem_src,
