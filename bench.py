@@ -47,13 +47,18 @@ KERNEL_SOURCES = ("flce_gemm.cuh", "flce_gemm_params.h", "ptx.cuh")
 
 
 def kernel_source_sha() -> str:
-    """sha256 over the GEMM kernel's sources: a DRAM-traffic figure measured with
-    ncu applies only while these are unchanged."""
+    """sha256 over the GEMM kernel's sources with comments and blank space
+    removed: a DRAM-traffic figure measured with ncu applies only while the code
+    is unchanged (editing a comment does not invalidate it)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "linear_cross_entropy_flce_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "linear_cross_entropy_flce_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                   # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,11 +8,12 @@
 //          2-5: in-SRAM tile product, online LogSumExp, immediate target
 //          extraction, no logits written).
 //   GRAD : Z recomputed tile by tile; the epilogue forms
-//          G = (exp(z - lse) - [v = y]) * scale in bf16 and writes one chunk of G
-//          (same page, 2. In-Kernel Gradient Computation: recompute the tile
-//          logits from the saved LSE, derive dL/dz in the kernel).
-//   F32  : plain product with an fp32 store, fp32 accumulate, or accumulate then
-//          round to bf16 — used for dW = G^T H and dH = G W (same page, 2.).
+//          G = (exp(z - lse) - [v = y]) * scale in bf16 and writes one chunk of G,
+//          stored chunk-major (same page, 2. In-Kernel Gradient Computation:
+//          recompute the tile logits from the saved LSE, derive dL/dz in the kernel).
+//   F32  : plain product whose tile is stored as fp32, added to fp32 already in
+//          memory, or stored as bf16 — used for dW = G^T H and dH = G W (same
+//          page, 2.).
 //
 // CTA layout (192 threads, one CTA per SM). kCta = 1: each CTA computes a
 // 128 x 256 tile. kCta = 2: a cluster pair computes a 256 x 256 tile with
@@ -27,9 +28,11 @@
 //                tcgen05.mma M x 256 x 16 steps into one of two TMEM accumulators
 //                and the commits).
 //   warps 2..5 : epilogue — warp w reads TMEM lanes 32*(w%4) .. +31, so each
-//                thread owns one output row of its CTA's 128 rows.
+//                thread owns one output row of its CTA's 128 rows; tiles that
+//                leave the SM go through per-warp 32 x 32 staging boxes in shared
+//                memory and TMA stores (or reduce-adds).
 // Every wait is bounded (see mbar_wait_bounded); on a timeout the CTA records
-// FLCE_ERR_TIMEOUT, the producer drains the copies it issued, the MMA thread
+// FLCE_ERR_TIMEOUT, the producer drains the copies it issued, the MMA warp
 // drains its MMAs, and both CTAs free TMEM and exit.
 #pragma once
 
