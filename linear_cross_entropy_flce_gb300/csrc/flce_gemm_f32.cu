@@ -34,7 +34,8 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
 cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const CUtensorMap& c, const GemmParams& p, int grid,
                             cudaStream_t stream) {
-  return cta_group == 2 ? launch<2>(a, b, c, p, grid, stream) : launch<1>(a, b, c, p, grid, stream);
+  if (cta_group != 2) return cudaErrorInvalidValue;  // only the pair kernel is built
+  return launch<2>(a, b, c, p, grid, stream);
 }
 
 }  // namespace flce

@@ -34,8 +34,8 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmParams&
 
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmParams& p, int grid, cudaStream_t stream, int fp8) {
-  if (fp8) return cta_group == 2 ? launch<2, 1>(a, b, p, grid, stream) : launch<1, 1>(a, b, p, grid, stream);
-  return cta_group == 2 ? launch<2, 0>(a, b, p, grid, stream) : launch<1, 0>(a, b, p, grid, stream);
+  if (cta_group != 2) return cudaErrorInvalidValue;  // only the pair kernel is built
+  return fp8 ? launch<2, 1>(a, b, p, grid, stream) : launch<2, 0>(a, b, p, grid, stream);
 }
 
 }  // namespace flce

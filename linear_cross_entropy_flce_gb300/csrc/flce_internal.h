@@ -11,7 +11,8 @@
 
 namespace flce {
 
-// cta_group 1: grid CTAs of one; cta_group 2: grid/2 clusters of two CTAs.
+// cta_group 2: grid/2 clusters of two CTAs (the kernel template also has a
+// one-CTA form, cta_group 1, which is not built; other values fail).
 // fp8 = 1: E4M3 operands (kind::f8f6f4) scaled by p.acc_scale in the epilogue.
 // c is the output map of the epilogue's TMA stores (unused by the LSE epilogue):
 // bf16 G for the gradient GEMM; fp32 (or bf16 for OUT_STORE_BF16) for the F32 one.
