@@ -174,3 +174,23 @@ def test_status_strings():
     for code in range(0, 10):
         assert flce.status_string(code) and flce.status_string(code) != "unknown status"
     assert flce.status_string(1234) == "unknown status"
+
+
+def test_header_compiles_as_c_and_links(tmp_path):
+    """A plain C99 program includes include/flce.h, links libflce.so and calls the
+    entry points that need no GPU (tests/abi_c_check.c)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(_binding.LIB_PATH)
+    exe = str(tmp_path / "abi_c_check")
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER),
+           os.path.join(here, "abi_c_check.c"), "-L", libdir, "-lflce",
+           "-Wl,-rpath," + libdir, "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
