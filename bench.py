@@ -553,22 +553,37 @@ def main(argv=None) -> int:
 
         run_e2e(args.warmup, 0)
         torch.cuda.synchronize(dev)
-        rep.barrier()
-        t0 = time.perf_counter()
-        ev0.record(copy_stream)
-        run_e2e(args.steps, args.warmup)
-        ev1.record(stream)
+        # one step's host-to-device copies on their own, for reference
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            bufs[1][0].copy_(H_host, non_blocking=True)
+            bufs[1][1].copy_(W_host, non_blocking=True)
+            bufs[1][2].copy_(y_host, non_blocking=True)
+        c1.record(copy_stream)
         torch.cuda.synchronize(dev)
-        wall = (time.perf_counter() - t0) / args.steps
+        h2d_alone_ms = c0.elapsed_time(c1)
+        rep.barrier()
+        with ClockSampler(local) as clk_e2e:
+            t0 = time.perf_counter()
+            ev0.record(copy_stream)
+            run_e2e(args.steps, args.warmup)
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            wall = (time.perf_counter() - t0) / args.steps
         rep.barrier()
         code = flce.check_status(status, stream.cuda_stream)
         if code != flce.FLCE_OK:
             raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
-        e2e_ms = rep.max(max(ev0.elapsed_time(ev1) / args.steps, 1e3 * wall))
+        ev_ms = ev0.elapsed_time(ev1) / args.steps
+        e2e_ms = rep.max(max(ev_ms, 1e3 * wall))
         h2d = H_host.numel() * 2 + W_host.numel() * 2 + y_host.numel() * 4
         e2e = {"value": N * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms,
-               "overlap": "copies of step i+1 on a second stream during step i"}
+               "overlap": "copies of step i+1 on a second stream during step i",
+               "ms_device_events": ev_ms, "ms_host_wall": 1e3 * wall,
+               "h2d_ms_one_step_alone": h2d_alone_ms,
+               "clocks": clk_e2e.summary()}
         del bufs
 
     flops = 8.0 * N * V * D
