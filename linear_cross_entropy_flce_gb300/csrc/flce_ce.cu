@@ -8,9 +8,9 @@
 //
 // Kernels:
 //   ce_count_kernel : one block; n_valid, label check, gradient scale.
-//   ce_rows_staged_kernel : rows of 64-768 KB. Persistent clusters of 1-8 CTAs,
+//   ce_rows_staged_kernel : rows of 64-880 KB. Persistent clusters of 1-8 CTAs,
 //                     one row per cluster at a time, each CTA's slice (at most
-//                     96 KB) copied into shared memory by the bulk-copy engine,
+//                     110 KB) copied into shared memory by the bulk-copy engine,
 //                     double-buffered so that the next row's slice streams in
 //                     while this one is reduced and its gradient written. Both
 //                     passes read shared memory: one DRAM read and one write per
@@ -316,10 +316,12 @@ __global__ void __launch_bounds__(kCeThreads)
 
 // ---- shared-memory staged variant ---------------------------------------------
 
-// Slices of at most 96 KB with one CTA per SM, or (bf16 rows, whose passes carry
-// twice the exponentials per byte) at most 56 KB with two CTAs per SM, so that
-// one CTA's reduction overlaps the other's gradient writes.
-constexpr int kSliceOne = 96 * 1024;
+// Slices of at most 110 KB with one CTA per SM (fp32 rows of 501 KB on clusters
+// of 5 rather than 6: more clusters resident, one barrier fewer per row), or
+// (bf16 rows, whose passes carry twice the exponentials per byte) at most 56 KB
+// with two CTAs per SM, so that one CTA's reduction overlaps the other's
+// gradient writes.
+constexpr int kSliceOne = 110 * 1024;
 constexpr int kSliceTwo = 56 * 1024;
 constexpr int kBulkPiece = 16 * 1024;      // bytes per bulk copy instruction
 
@@ -641,7 +643,7 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
                            int N, int V, int ignore_index, const float* scale, float* lse,
                            float* nll, void* g, int64_t gld_bytes, int sms, int32_t* status,
                            int64_t timeout_ns, cudaStream_t stream) {
-  // Rows of 64-768 KB: slices staged in shared memory by a cluster of
+  // Rows of 64-880 KB: slices staged in shared memory by a cluster of
   // ceil(row / slice) CTAs (at most eight).
   const int64_t vec_bytes = static_cast<int64_t>(V / (bf16 ? 8 : 4)) * 16;
   auto cluster_for = [&](int64_t slice) -> int {

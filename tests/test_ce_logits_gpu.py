@@ -129,10 +129,10 @@ def test_matches_fused_loss_on_the_same_logits():
 
 
 @pytest.mark.parametrize("N,V,bf16", [
-    (40, 128256, False),   # 501 KB rows: staged slices, cluster of 6
+    (40, 128256, False),   # 501 KB rows: staged slices, cluster of 5
     (24, 128257, True),    # 250 KB bf16 rows with a scalar tail: staged, cluster of 3
-    (9, 100003, False),    # staged, ragged fp32 tail
-    (5, 200003, False),    # 781 KB rows: streamed kernel, cluster of 4
+    (9, 100003, False),    # staged (cluster of 4), ragged fp32 tail
+    (4, 240007, False),    # 938 KB rows: streamed kernel, cluster of 4
 ])
 def test_long_rows_parity_and_in_place(N, V, bf16):
     """Rows long enough for multi-CTA clusters (shared-memory staged slices, or
