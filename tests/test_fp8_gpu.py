@@ -53,3 +53,19 @@ def test_fp8_forward_only_and_llama2_workload():
     errs = compare(full, ref)
     print(errs)
     assert_within(errs)
+
+
+@pytest.mark.parametrize("opts", [{"v_chunk": 512, "n_block": 256},
+                                  {"v_chunk": 768, "n_block": 128, "dw_dtype": "bfloat16"}])
+def test_fp8_token_blocks_and_chunks(opts):
+    """The FP8 variant under plans with several vocabulary chunks and token
+    blocks (dH accumulated over chunks, dW over token blocks, bf16 dW)."""
+    wl = flce_inputs.Workload("fp8plan", 300, 200 + 56, 1500, 1.0, 0.05, "uniform", 0.07, seed=5)
+    (H8, sh, W8, sw, lab, H, W), (He, We, Hb, Wb, y) = _case(wl)
+    res = flce.forward_backward_fp8(H8, sh, W8, sw, lab, H, W, **opts)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
+                      Wg=flce_inputs.bf16_bits_to_f64(Wb))
+    errs = compare(res, ref)
+    print(errs)
+    assert_within(errs)
