@@ -172,20 +172,42 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
  * The gradient products take the bf16 tensors the FP8 operands were made from:
  * dH = G W and dW = G^T H (straight through the quantisation).
  *   H8 [N, D], W8 [V, D]  E4M3 bytes, row-major, 16-byte aligned, D % 16 == 0
- *   scale_h, scale_w      positive fp32 scales (dequantised value = scale * e4m3)
+ *   scale_h, scale_w      device pointers, each to one positive finite fp32 scale
+ *                         (dequantised value = scale * e4m3), read by the kernels,
+ *                         so a scale computed on the device (flce_quantize_e4m3)
+ *                         needs no host round trip; 4-byte aligned
  *   H, W                  bf16 [N, D], [V, D] (flce_forward_backward_fp8 only)
  * Other arguments, outputs, workspace (flce_workspace_size) and errors as in
  * flce_forward / flce_forward_backward.
  */
-int flce_forward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+int flce_forward_fp8(const uint8_t* H8, const float* scale_h, const uint8_t* W8,
+                     const float* scale_w,
                      const int32_t* labels, int64_t N, int64_t D, int64_t V,
                      const flce_options* opt, float* loss, float* lse, void* workspace,
                      size_t ws_bytes, int32_t* status, void* stream);
-int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+int flce_forward_backward_fp8(const uint8_t* H8, const float* scale_h, const uint8_t* W8,
+                              const float* scale_w,
                               const uint16_t* H, const uint16_t* W, const int32_t* labels,
                               int64_t N, int64_t D, int64_t V, const flce_options* opt,
                               float* loss, float* lse, uint16_t* dH, void* dW, void* workspace,
                               size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Per-tensor E4M3 quantisation on the device: the operand preparation the FP8
+ * variant expects (the reading of the lecture notes' FP8 question that the FP8
+ * entry points follow). Over the bf16 tensor x [n]:
+ *     amax  = max_i |x_i|
+ *     scale = amax / 448, computed in double and rounded to fp32 (1 if amax == 0)
+ *     q_i   = e4m3(x_i / scale), the division in fp32, rounded to the nearest
+ *             code (ties to the even code), saturating at +-448; a zero result
+ *             is encoded as +0
+ * writes q (uint8 [n]), out[0] = scale and out[1] = amax (two device floats, the
+ * first usable directly as scale_h / scale_w of the FP8 entry points). x must be
+ * finite. n % 8 == 0, x and q 16-byte aligned, out 8-byte aligned. Enqueues a
+ * 4-byte reset and two kernels on `stream`; no host synchronisation, no
+ * allocation. Errors: FLCE_ERR_NULL, FLCE_ERR_SHAPE (n < 1), FLCE_ERR_ALIGN.
+ */
+int flce_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, float* out, void* stream);
 
 /*
  * flce_forward, for callers that cannot allocate device memory at call time and

@@ -90,15 +90,17 @@ lib.flce_ce_logits.argtypes = [_vp, ctypes.c_int32, _i64, _vp, _i64, _i64, ctype
                                _vp, _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_ce_logits.restype = ctypes.c_int
 _f32 = ctypes.c_float
-lib.flce_forward_fp8.argtypes = [_vp, _f32, _vp, _f32, _vp, _i64, _i64, _i64,
+lib.flce_forward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                  ctypes.POINTER(Options), _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_forward_fp8.restype = ctypes.c_int
-lib.flce_forward_backward_fp8.argtypes = [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i64,
+lib.flce_forward_backward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                           ctypes.POINTER(Options), _vp, _vp, _vp, _vp, _vp,
                                           ctypes.c_size_t, _vp, _vp]
 lib.flce_forward_backward_fp8.restype = ctypes.c_int
 lib.flce_scale_grads.argtypes = [_vp, _i64, _vp, _i64, ctypes.c_int32, _vp, _vp]
 lib.flce_scale_grads.restype = ctypes.c_int
+lib.flce_quantize_e4m3.argtypes = [_vp, _i64, _vp, _vp, _vp]
+lib.flce_quantize_e4m3.restype = ctypes.c_int
 lib.flce_check_status.argtypes = [_vp, _vp]
 lib.flce_check_status.restype = ctypes.c_int
 lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -320,12 +322,46 @@ def ce_logits(logits, labels, *, need_grad: bool = True, in_place: bool = False,
     return r
 
 
-def forward_backward_fp8(H8, scale_h: float, W8, scale_w: float, labels, H=None, W=None, *,
+def _device_scale(scale, dev):
+    """A per-tensor scale as a device fp32 scalar: a CUDA float32 tensor whose first
+    element is the scale (e.g. out[0] of quantize_e4m3), or a Python number."""
+    import torch
+    if isinstance(scale, torch.Tensor):
+        if not (scale.is_cuda and scale.dtype == torch.float32 and scale.numel() >= 1
+                and scale.is_contiguous()):
+            raise TypeError("a scale tensor must be a contiguous CUDA float32 tensor")
+        return scale
+    return torch.tensor([float(scale)], dtype=torch.float32, device=dev)
+
+
+def quantize_e4m3(x, *, out=None, q=None, stream=None):
+    """Per-tensor E4M3 quantisation of a bf16 CUDA tensor on the device via
+    flce_quantize_e4m3: returns (q uint8 with x's shape, out float32[2] holding
+    [scale, amax]); out[0:1] serves directly as a scale of the FP8 entry points."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous bf16 CUDA tensor")
+    dev = x.device
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(2, dtype=torch.float32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_quantize_e4m3(_ptr(x), x.numel(), _ptr(q), _ptr(out), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_quantize_e4m3")
+    return q, out
+
+
+def forward_backward_fp8(H8, scale_h, W8, scale_w, labels, H=None, W=None, *,
                          need_dh: bool = True, need_dw: bool = True, out: Optional[dict] = None,
                          workspace=None, status=None, stream=None, **options) -> Result:
     """FP8 operand variant (flce_forward_backward_fp8, or flce_forward_fp8 when no
     gradient is requested): E4M3 H8 [N, D] and W8 [V, D] (torch.uint8) with
-    per-tensor scales define the logits; the gradient products use bf16 H, W."""
+    per-tensor scales define the logits; the gradient products use bf16 H, W.
+    scale_h / scale_w: Python numbers or CUDA float32 tensors (the device scalar
+    at element 0 is read by the kernels)."""
     import torch
     grads = need_dh or need_dw
     if not (H8.is_cuda and W8.is_cuda and labels.is_cuda):
@@ -342,6 +378,8 @@ def forward_backward_fp8(H8, scale_h: float, W8, scale_w: float, labels, H=None,
         _check_inputs(H, W, labels)
     opts = make_options(**options)
     dev = H8.device
+    sh = _device_scale(scale_h, dev)
+    sw = _device_scale(scale_w, dev)
     out = dict(out or {})
     loss = out.get("loss")
     if loss is None:
@@ -366,11 +404,11 @@ def forward_backward_fp8(H8, scale_h: float, W8, scale_w: float, labels, H=None,
     wsb = workspace.numel() * workspace.element_size()
     if grads:
         rc = lib.flce_forward_backward_fp8(
-            _ptr(H8), float(scale_h), _ptr(W8), float(scale_w), _ptr(H), _ptr(W), _ptr(labels),
+            _ptr(H8), _ptr(sh), _ptr(W8), _ptr(sw), _ptr(H), _ptr(W), _ptr(labels),
             N, D, V, ctypes.byref(opts), _ptr(loss), _ptr(lse), _ptr(dH) if need_dh else None,
             _ptr(dW) if need_dw else None, _ptr(workspace), wsb, _ptr(status), stream)
     else:
-        rc = lib.flce_forward_fp8(_ptr(H8), float(scale_h), _ptr(W8), float(scale_w),
+        rc = lib.flce_forward_fp8(_ptr(H8), _ptr(sh), _ptr(W8), _ptr(sw),
                                   _ptr(labels), N, D, V, ctypes.byref(opts), _ptr(loss),
                                   _ptr(lse), _ptr(workspace), wsb, _ptr(status), stream)
     if rc != FLCE_OK:

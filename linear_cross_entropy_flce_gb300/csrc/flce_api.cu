@@ -283,7 +283,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Fp8Operands {
   const uint8_t* H8 = nullptr;
   const uint8_t* W8 = nullptr;
-  float scale_h = 1.f, scale_w = 1.f;
+  const float* scale_h = nullptr;  // device fp32 scalars
+  const float* scale_w = nullptr;
 };
 
 // uint8 matrix [outer][inner] read in boxes of box_inner x box_outer bytes with
@@ -323,8 +324,10 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   rc = check_options(o);
   if (rc != FLCE_OK) return rc;
   if (fp8 && (D % 16 != 0 || !aligned16(f8.H8) || !aligned16(f8.W8))) return FLCE_ERR_ALIGN;
-  if (fp8 && !(f8.scale_h > 0.f && f8.scale_w > 0.f && f8.scale_h * f8.scale_w < 3.0e38f))
-    return FLCE_ERR_OPTION;
+  if (fp8 && (f8.scale_h == nullptr || f8.scale_w == nullptr)) return FLCE_ERR_NULL;
+  if (fp8 && ((reinterpret_cast<uintptr_t>(f8.scale_h) & 3u) ||
+              (reinterpret_cast<uintptr_t>(f8.scale_w) & 3u)))
+    return FLCE_ERR_ALIGN;
   if ((H && !aligned16(H)) || (W && !aligned16(W)) || !aligned16(labels) ||
       !aligned16(workspace) ||
       (lse_out && !aligned16(lse_out)) || (dH && !aligned16(dH)) || (dW && !aligned16(dW)) ||
@@ -385,7 +388,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   }
   const int k_blocks_z = static_cast<int>(ceil_div(D, fp8 ? 2 * BK : BK));
   const uint32_t idesc_z = fp8 ? make_idesc_e4m3_f32(P.tile_m, BN) : make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
-  const float acc_scale = fp8 ? f8.scale_h * f8.scale_w : 1.f;
+
 
   // ---- 1. forward LSE GEMM ----
   GemmParams g{};
@@ -394,7 +397,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   g.m_blocks = P.m_blocks;
   g.n_blocks = P.v_tiles;
   g.k_blocks = k_blocks_z;
-  g.acc_scale = acc_scale;
+  g.acc_scale_h = f8.scale_h;
+  g.acc_scale_w = f8.scale_w;
   g.splits = P.splits;
   g.part_stride = P.part_stride;
   g.num_units = P.splits * P.m_blocks;
@@ -464,7 +468,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
       q.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
       q.n_blocks = static_cast<int>(ceil_div(c_len, BN));
       q.k_blocks = k_blocks_z;
-      q.acc_scale = acc_scale;
+      q.acc_scale_h = f8.scale_h;
+      q.acc_scale_w = f8.scale_w;
       q.num_units = q.m_blocks * q.n_blocks;
       q.group_m = std::min(q.m_blocks, 16);
       q.idesc = idesc_z;
@@ -738,7 +743,8 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
                    false, workspace, ws_bytes, status, stream);
 }
 
-int flce_forward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+int flce_forward_fp8(const uint8_t* H8, const float* scale_h, const uint8_t* W8,
+                     const float* scale_w,
                      const int32_t* labels, int64_t N, int64_t D, int64_t V,
                      const flce_options* opt, float* loss, float* lse, void* workspace,
                      size_t ws_bytes, int32_t* status, void* stream) {
@@ -751,7 +757,8 @@ int flce_forward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float 
                    workspace, ws_bytes, status, stream);
 }
 
-int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W8, float scale_w,
+int flce_forward_backward_fp8(const uint8_t* H8, const float* scale_h, const uint8_t* W8,
+                              const float* scale_w,
                               const uint16_t* H, const uint16_t* W, const int32_t* labels,
                               int64_t N, int64_t D, int64_t V, const flce_options* opt,
                               float* loss, float* lse, uint16_t* dH, void* dW, void* workspace,
@@ -763,6 +770,21 @@ int flce_forward_backward_fp8(const uint8_t* H8, float scale_h, const uint8_t* W
   f8.scale_w = scale_w;
   return flce::run(H, W, f8, labels, N, D, V, opt, loss, lse, dH, dW, true, workspace, ws_bytes,
                    status, stream);
+}
+
+int flce_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, float* out, void* stream) {
+  if (x == nullptr || q == nullptr || out == nullptr) return FLCE_ERR_NULL;
+  if (n < 1) return FLCE_ERR_SHAPE;
+  if (n % 8 != 0 || !flce::aligned16(x) || !flce::aligned16(q) ||
+      (reinterpret_cast<uintptr_t>(out) & 7u))
+    return FLCE_ERR_ALIGN;
+  int sms = 0;
+  const int rc = flce::device_info(&sms);
+  if (rc != FLCE_OK) return rc;
+  return flce::launch_quantize_e4m3(x, n, q, out, sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FLCE_OK
+             : FLCE_ERR_CUDA;
 }
 
 int flce_scale_grads(uint16_t* dH, int64_t dh_elems, void* dW, int64_t dw_elems,

@@ -166,7 +166,8 @@ __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, 
 
 // kFp8 = 1: A and B are E4M3 bytes (K-major only), 128 of them per 128-byte
 // stage row, multiplied with tcgen05 kind::f8f6f4; the epilogue scales z by
-// p.acc_scale. The shared-memory image of a stage is the same as for bf16.
+// the product of the two device scales. The shared-memory image of a stage is
+// the same as for bf16.
 template <int kEpi, int kCta, int kFp8 = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -428,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float scale_v = 0.f;
     if constexpr (kEpi == EPI_GRAD) scale_v = *p.scale;
+    float acc_scale = 1.f;  // FP8 operands: product of the two per-tensor scales
+    if constexpr (kFp8) acc_scale = *p.acc_scale_h * *p.acc_scale_w;
     // this warp's two staging boxes, used alternately
     const uint32_t stg = stage0 + Cfg::kRingBytes + static_cast<uint32_t>(quarter) * 2u * Cfg::kStgBytes;
     uint32_t nbox = 0;
@@ -485,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
           if constexpr (kFp8) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] *= p.acc_scale;
+            for (int k = 0; k < 32; ++k) v[k] *= acc_scale;
           }
           const int col = n_blk * BN + c * 32;  // product column
           if constexpr (kEpi == EPI_LSE) {

@@ -88,7 +88,10 @@ struct GemmParams {
                 // walk the vocabulary ranges together)
   int a_hint, b_hint;  // L2 policy of the A / B loads: 0 none, 1 evict_first, 2 evict_last
   uint32_t idesc;
-  float acc_scale;   // FP8 operands: z = acc_scale * accumulator (scale_h * scale_w)
+  // FP8 operands: z = scale_h * scale_w * accumulator, the two scales read from
+  // device memory once per epilogue thread
+  const float* acc_scale_h;
+  const float* acc_scale_w;
   int64_t timeout_ns;
   int32_t* status;
   int m_valid;  // rows of the product that exist

@@ -13,7 +13,8 @@ namespace flce {
 
 // cta_group 2: grid/2 clusters of two CTAs (the kernel template also has a
 // one-CTA form, cta_group 1, which is not built; other values fail).
-// fp8 = 1: E4M3 operands (kind::f8f6f4) scaled by p.acc_scale in the epilogue.
+// fp8 = 1: E4M3 operands (kind::f8f6f4) scaled in the epilogue by the product of
+// the device scales p.acc_scale_h, p.acc_scale_w.
 // c is the output map of the epilogue's TMA stores (unused by the LSE epilogue):
 // bf16 G for the gradient GEMM; fp32 (or bf16 for OUT_STORE_BF16) for the F32 one.
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
@@ -53,6 +54,11 @@ cudaError_t launch_ce_rows(int bf16, const void* z, int64_t ld_bytes, const int3
 // dst[i] = bf16(src[i]) (round to nearest even), n a multiple of 8, both 16-byte aligned.
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, int sms,
                                cudaStream_t stream);
+
+// E4M3 per-tensor quantisation of bf16 x [n] (n % 8 == 0): out[1] = amax,
+// out[0] = scale, q = e4m3(x / scale).
+cudaError_t launch_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, float* out, int sms,
+                                 cudaStream_t stream);
 
 // x (bf16 if bf16, else fp32; bytes a multiple of 16) *= *scale, in place.
 cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, int sms,

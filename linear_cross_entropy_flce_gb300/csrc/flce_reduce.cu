@@ -143,7 +143,87 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint4* __rest
   }
 }
 
+// ---- per-tensor E4M3 quantisation -----------------------------------------------
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// amax over |x|: grid-stride over 8-element vectors, warp then block max, one
+// atomicMax per block on the bits of a non-negative float (ordered like the value).
+__global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, unsigned int* amax_bits) {
+  __shared__ float s_w[32];
+  float m = 0.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 v = x[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] & 0xFFFFu)));
+      m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_w[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < static_cast<int>(blockDim.x >> 5) ? s_w[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) atomicMax(amax_bits, __float_as_uint(m));
+  }
+}
+
+// Two fp32 values to two E4M3 bytes (round to nearest even, saturating), low byte
+// first; a zero result is +0.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  uint32_t b = r;
+  if ((b & 0x007Fu) == 0) b &= 0xFF00u;
+  if ((b & 0x7F00u) == 0) b &= 0x00FFu;
+  return b;
+}
+
+// q = e4m3(x / scale) with scale = amax / 448 (double, rounded to fp32; 1 if
+// amax == 0); block 0 stores the scale next to the amax.
+__global__ void quantize_e4m3_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ q,
+                                     float* out) {
+  const float amax = __ldcg(out + 1);
+  const float scale = amax > 0.f ? static_cast<float>(static_cast<double>(amax) / 448.0) : 1.f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) out[0] = scale;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 v = x[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      b[k] = e4m3x2(__fdiv_rn(bf16_bits_to_float(w[k] & 0xFFFFu), scale),
+                    __fdiv_rn(bf16_bits_to_float(w[k] >> 16), scale));
+    q[i] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, float* out, int sms,
+                                 cudaStream_t stream) {
+  const int64_t n8 = n / 8;
+  cudaError_t e = cudaMemsetAsync(out + 1, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const int64_t want = (n8 + threads - 1) / threads;
+  const int grid = static_cast<int>(want < static_cast<int64_t>(sms) * 8 ? want : static_cast<int64_t>(sms) * 8);
+  amax_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(x), n8,
+                                            reinterpret_cast<unsigned int*>(out + 1));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quantize_e4m3_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(x), n8,
+                                                     reinterpret_cast<uint2*>(q), out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, int sms,
                                cudaStream_t stream) {

@@ -24,7 +24,8 @@ def test_header_declares_the_abi():
     assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
                             "flce_ce_workspace_size", "flce_ce_logits", "flce_forward_fp8",
-                            "flce_forward_backward_fp8", "flce_scale_grads",
+                            "flce_forward_backward_fp8", "flce_quantize_e4m3",
+                            "flce_scale_grads",
                             "flce_check_status", "flce_status_string"])
 
 
@@ -141,8 +142,8 @@ def test_ce_logits_host_rejections():
 
 def test_fp8_host_rejections():
     f = flce.lib.flce_forward_fp8
-    ok = dict(H8=0x1000, sh=1.0, W8=0x2000, sw=1.0, y=0x3000, N=64, D=128, V=1000, loss=0x4000,
-              ws=0x5000)
+    ok = dict(H8=0x1000, sh=0x8000, W8=0x2000, sw=0x8004, y=0x3000, N=64, D=128, V=1000,
+              loss=0x4000, ws=0x5000)
 
     def call(**kw):
         a = dict(ok, **kw)
@@ -153,12 +154,25 @@ def test_fp8_host_rejections():
     assert call(W8=None) == flce.FLCE_ERR_NULL
     assert call(D=136) == flce.FLCE_ERR_ALIGN      # D % 16 != 0 for E4M3 rows
     assert call(H8=0x1004) == flce.FLCE_ERR_ALIGN
-    assert call(sh=0.0) == flce.FLCE_ERR_OPTION
-    assert call(sw=-1.0) == flce.FLCE_ERR_OPTION
+    assert call(sh=None) == flce.FLCE_ERR_NULL     # scales are device fp32 scalars
+    assert call(sw=None) == flce.FLCE_ERR_NULL
+    assert call(sh=0x8002) == flce.FLCE_ERR_ALIGN
     g = flce.lib.flce_forward_backward_fp8
     # the gradient products need the bf16 operands
-    assert g(0x1000, 1.0, 0x2000, 1.0, None, None, 0x3000, 64, 128, 1000, None, 0x4000, None,
-             0x6000, 0x7000, 0x5000, 1 << 30, None, None) == flce.FLCE_ERR_NULL
+    assert g(0x1000, 0x8000, 0x2000, 0x8004, None, None, 0x3000, 64, 128, 1000, None, 0x4000,
+             None, 0x6000, 0x7000, 0x5000, 1 << 30, None, None) == flce.FLCE_ERR_NULL
+
+
+def test_quantize_e4m3_host_rejections():
+    f = flce.lib.flce_quantize_e4m3
+    assert f(None, 64, 0x2000, 0x3000, None) == flce.FLCE_ERR_NULL
+    assert f(0x1000, 64, None, 0x3000, None) == flce.FLCE_ERR_NULL
+    assert f(0x1000, 64, 0x2000, None, None) == flce.FLCE_ERR_NULL
+    assert f(0x1000, 0, 0x2000, 0x3000, None) == flce.FLCE_ERR_SHAPE
+    assert f(0x1000, 12, 0x2000, 0x3000, None) == flce.FLCE_ERR_ALIGN   # n % 8 != 0
+    assert f(0x1008, 64, 0x2000, 0x3000, None) == flce.FLCE_ERR_ALIGN
+    assert f(0x1000, 64, 0x2008, 0x3000, None) == flce.FLCE_ERR_ALIGN
+    assert f(0x1000, 64, 0x2000, 0x3004, None) == flce.FLCE_ERR_ALIGN
 
 
 def test_scale_grads_host_rejections():

@@ -69,3 +69,66 @@ def test_fp8_token_blocks_and_chunks(opts):
     errs = compare(res, ref)
     print(errs)
     assert_within(errs)
+
+
+def _quantize_expected(bits):
+    """Per-tensor E4M3 quantisation as flce_quantize_e4m3 states it: scale = amax / 448
+    rounded to fp32 (1 for an all-zero tensor), the quotient x / scale in fp32, then
+    the nearest E4M3 code (flce_inputs.e4m3_encode)."""
+    x = flce_inputs.bf16_bits_to_f32(bits).astype(np.float32)
+    amax = np.float32(np.max(np.abs(x)))
+    scale = np.float32(float(amax) / 448.0) if amax > 0 else np.float32(1.0)
+    y = (x / scale).astype(np.float32)
+    return flce_inputs.e4m3_encode(y.astype(np.float64)), scale, amax
+
+
+def _wide_range_bf16(shape, seed):
+    """bf16 bits spanning E4M3's whole range after scaling: N(0,1) times 10^u,
+    u uniform in [-7, 1], so codes land in the subnormals, the normals and at 448."""
+    g = np.random.default_rng(seed)
+    x = g.standard_normal(shape).astype(np.float32) * np.float32(10.0) ** g.uniform(-7, 1, shape).astype(np.float32)
+    return flce_inputs.f32_to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("case", ["normal", "wide", "zeros", "tiny", "ragged_grid"])
+def test_device_quantizer_matches_its_definition(case):
+    if case == "normal":
+        bits = flce_inputs.normal_bf16((300, 256), 0.05, seed=3, stream=0)
+    elif case == "wide":
+        bits = _wide_range_bf16((517, 96), seed=4)
+    elif case == "zeros":
+        bits = np.zeros((16, 64), dtype=np.uint16)
+        bits[3, 5] = 0x8000  # -0 counts as zero
+    elif case == "tiny":
+        bits = flce_inputs.normal_bf16((1, 8), 1.0, seed=5, stream=0)
+    else:  # more 8-element groups than one grid pass covers
+        bits = _wide_range_bf16((4099, 2056), seed=6)
+    q_ref, scale_ref, amax_ref = _quantize_expected(bits)
+    x = torch.from_numpy(bits.view(np.int16)).to("cuda:0").view(torch.bfloat16)
+    q, out = flce.quantize_e4m3(x)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert o[1] == amax_ref and o[0] == scale_ref, (o, amax_ref, scale_ref)
+    qd = q.cpu().numpy()
+    bad = np.flatnonzero(qd.ravel() != q_ref.ravel())
+    assert bad.size == 0, (bad[:8], qd.ravel()[bad[:8]], q_ref.ravel()[bad[:8]])
+
+
+def test_device_quantized_operands_feed_the_fp8_path():
+    """H8, W8 and their scales made on the device (scales passed as device scalars,
+    no host round trip) give the oracle's result over the dequantised operands."""
+    wl = flce_inputs.Workload("fp8q", 300, 256, 3000, 1.0, 0.05, "uniform", 0.07, seed=11)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H, W, lab = to_device(Hb, Wb, y)
+    H8, oh = flce.quantize_e4m3(H)
+    W8, ow = flce.quantize_e4m3(W)
+    res = flce.forward_backward_fp8(H8, oh[0:1], W8, ow[0:1], lab, H, W)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    torch.cuda.synchronize()
+    He = flce_inputs.e4m3_decode(H8.cpu().numpy()) * np.float64(oh[0].item())
+    We = flce_inputs.e4m3_decode(W8.cpu().numpy()) * np.float64(ow[0].item())
+    ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
+                      Wg=flce_inputs.bf16_bits_to_f64(Wb))
+    errs = compare(res, ref)
+    print(errs)
+    assert_within(errs)
