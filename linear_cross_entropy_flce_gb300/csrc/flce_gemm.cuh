@@ -22,7 +22,9 @@
 //   warp 0     : TMA producer (each CTA; all lanes wait, one elected lane issues)
 //                — streams the CTA's A rows and B half, K-slice by K-slice, into a
 //                ring of shared-memory stages; the copies of both CTAs complete on
-//                the even CTA's stage barrier.
+//                the even CTA's stage barrier. With k_serpentine, every second tile
+//                of a pair walks K from the end, so that it starts on the K slices
+//                the tiles before it read last, which are the ones still in L2.
 //   warp 1     : TMEM allocator (both CTAs) and MMA issuer (the even CTA's warp:
 //                all lanes wait on the barriers, one elected lane issues the
 //                tcgen05.mma M x 256 x 16 steps into one of two TMEM accumulators
@@ -241,11 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t pol_a = make_l2_policy(p.a_hint);
       const uint64_t pol_b = make_l2_policy(p.b_hint);
+      int tile_it = 0;
       for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         int m_blk, n_begin, n_end;
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
-        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
-          for (int ks = 0; ks < k_stages; ++ks) {
+        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk, ++tile_it) {
+          const bool k_rev = p.k_serpentine && (tile_it & 1);
+          for (int kq = 0; kq < k_stages; ++kq) {
+            const int ks = k_rev ? k_stages - 1 - kq : kq;   // K block group this stage holds
             const bool empty_ok = mbar_wait_bounded<kCl>(empty_bar(stage), phase ^ 1u, tmo, abort_flag);
             if (!__all_sync(0xffffffffu, empty_ok)) {  // one decision for the whole warp
               ok = false;
@@ -338,10 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool issued_any = false;
       const bool a_mn = p.a_mn_major != 0, b_mn = p.b_mn_major != 0;
+      int tile_it = 0;
       for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         int m_blk, n_begin, n_end;
         unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
-        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk) {
+        for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk, ++tile_it) {
+          const bool k_rev = p.k_serpentine && (tile_it & 1);
           // both CTAs' epilogues must have drained this accumulator
           bool got;
           if constexpr (kCta == 2) {
@@ -361,13 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int ks = 0; ks < k_stages; ++ks) {
+          for (int kq = 0; kq < k_stages; ++kq) {
             const bool full_ok = mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag);
             if (!__all_sync(0xffffffffu, full_ok)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            const int ks = k_rev ? k_stages - 1 - kq : kq;   // as the producer loaded it
             const int nsub = min(kSub, p.k_blocks - ks * kSub);
             if (elect_one()) {
 #pragma unroll
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
                 const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
                                          : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
-                const uint32_t accum = (ks | sub | k) != 0 ? 1u : 0u;
+                const uint32_t accum = (kq | sub | k) != 0 ? 1u : 0u;   // first MMA of the tile overwrites
                 if constexpr (kFp8) umma_f8_cg<kCta>(d_tmem, da, db, p.idesc, accum);
                 else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, accum);
               }

@@ -84,6 +84,7 @@ struct GemmParams {
   int num_units;
   int splits;   // EPI_LSE: vocabulary ranges per row block
   int part_stride;  // EPI_LSE: 128-row blocks per vocabulary range in `part`
+  int k_serpentine;  // 1: each CTA pair walks K backwards on every second tile it runs
   int group_m;  // tile raster: groups of group_m row blocks (EPI_LSE: units of a group
                 // walk the vocabulary ranges together)
   int a_hint, b_hint;  // L2 policy of the A / B loads: 0 none, 1 evict_first, 2 evict_last
