@@ -128,6 +128,14 @@ def test_dw_columns_sum_to_zero():
     assert float((colsum.abs() / scale).max()) < 5e-3
 
 
+def test_several_tiles_per_pair_and_partial_last_k_stage():
+    """dW and dH launches with more tiles than the 76 cluster pairs, so that pairs run
+    tiles in both K directions, and K extents (2460 tokens; a 9760-id last chunk) that
+    leave the last ring stage half filled."""
+    Hb, Wb, y = _inputs(2460, 2048, 20000, seed=21, p_ignore=0.05)
+    _run_and_compare(Hb, Wb, y, v_chunk=10240)
+
+
 def test_run_to_run_bitwise_determinism():
     Hb, Wb, y = _inputs(700, 512, 5000, seed=15, p_ignore=0.05)
     H, W, lab = to_device(Hb, Wb, y)
