@@ -175,7 +175,10 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
  *   scale_h, scale_w      device pointers, each to one positive finite fp32 scale
  *                         (dequantised value = scale * e4m3), read by the kernels,
  *                         so a scale computed on the device (flce_quantize_e4m3)
- *                         needs no host round trip; 4-byte aligned
+ *                         needs no host round trip; 4-byte aligned. Only the
+ *                         pointers are checked (FLCE_ERR_NULL, FLCE_ERR_ALIGN):
+ *                         the values are read on the device, and a scale that
+ *                         is not positive and finite gives meaningless outputs
  *   H, W                  bf16 [N, D], [V, D] (flce_forward_backward_fp8 only)
  * Other arguments, outputs, workspace (flce_workspace_size) and errors as in
  * flce_forward / flce_forward_backward.

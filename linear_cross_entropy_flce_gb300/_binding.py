@@ -89,7 +89,6 @@ lib.flce_ce_workspace_size.restype = ctypes.c_int
 lib.flce_ce_logits.argtypes = [_vp, ctypes.c_int32, _i64, _vp, _i64, _i64, ctypes.POINTER(Options),
                                _vp, _vp, _vp, _i64, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_ce_logits.restype = ctypes.c_int
-_f32 = ctypes.c_float
 lib.flce_forward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                  ctypes.POINTER(Options), _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 lib.flce_forward_fp8.restype = ctypes.c_int
