@@ -119,17 +119,19 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
 
 
 def to_fp8_per_tensor(x_bf16_bits: np.ndarray, block_rows: int = 8192):
-    """Per-tensor amax scaling of a bf16 tensor into E4M3: scale = amax / 448 rounded
-    to float32 (1 for an all-zero tensor) and codes = e4m3(x / scale), the quotient
+    """Per-tensor amax scaling of a bf16 tensor into E4M3: scale = amax / 448 and
+    inv = 448 / amax, each rounded to float32 (inv capped at the largest finite
+    float32; both 1 for an all-zero tensor), and codes = e4m3(x * inv), the product
     taken in float32. Returns (uint8 codes, float32 scale)."""
     amax = 0.0
     for r0 in range(0, x_bf16_bits.shape[0], block_rows):
         amax = max(amax, float(np.max(np.abs(bf16_bits_to_f32(x_bf16_bits[r0:r0 + block_rows])))))
     scale = np.float32(amax / 448.0 if amax > 0 else 1.0)
+    inv = np.float32(min(448.0 / amax, float(np.finfo(np.float32).max)) if amax > 0 else 1.0)
     out = np.empty(x_bf16_bits.shape, dtype=np.uint8)
     for r0 in range(0, x_bf16_bits.shape[0], block_rows):
         blk = bf16_bits_to_f32(x_bf16_bits[r0:r0 + block_rows]).astype(np.float32)
-        out[r0:r0 + block_rows] = e4m3_encode((blk / scale).astype(np.float64))
+        out[r0:r0 + block_rows] = e4m3_encode((blk * inv).astype(np.float64))
     return out, scale
 
 

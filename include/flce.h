@@ -201,7 +201,10 @@ int flce_forward_backward_fp8(const uint8_t* H8, const float* scale_h, const uin
  * entry points follow). Over the bf16 tensor x [n]:
  *     amax  = max_i |x_i|
  *     scale = amax / 448, computed in double and rounded to fp32 (1 if amax == 0)
- *     q_i   = e4m3(x_i / scale), the division in fp32, rounded to the nearest
+ *     inv   = 448 / amax, computed in double, rounded to fp32 and capped at the
+ *             largest finite fp32 (reached only for amax below about 1.3e-36;
+ *             1 if amax == 0)
+ *     q_i   = e4m3(x_i * inv), the product in fp32, rounded to the nearest
  *             code (ties to the even code), saturating at +-448; a zero result
  *             is encoded as +0
  * writes q (uint8 [n]), out[0] = scale and out[1] = amax (two device floats, the

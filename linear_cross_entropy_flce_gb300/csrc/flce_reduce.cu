@@ -147,21 +147,30 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint4* __rest
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// amax over |x|: grid-stride over 8-element vectors, warp then block max, one
-// atomicMax per block on the bits of a non-negative float (ordered like the value).
+// amax over |x|: grid-stride over 8-element vectors, four independent 16-byte
+// loads in flight per thread, warp then block max, one atomicMax per block on the
+// bits of a non-negative float (ordered like the value). Plain loads, so that a
+// tensor smaller than L2 is still there for the quantising pass.
+__device__ __forceinline__ float absmax8(uint4 v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] & 0xFFFFu)));
+    m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] >> 16)));
+  }
+  return m;
+}
+
 __global__ void amax_kernel(const uint4* __restrict__ x, int64_t n8, unsigned int* amax_bits) {
   __shared__ float s_w[32];
   float m = 0.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const uint4 v = x[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] & 0xFFFFu)));
-      m = fmaxf(m, fabsf(bf16_bits_to_float(w[k] >> 16)));
-    }
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = x[i], b = x[i + stride], c = x[i + 2 * stride], d = x[i + 3 * stride];
+    m = absmax8(d, absmax8(c, absmax8(b, absmax8(a, m))));
   }
+  for (; i < n8; i += stride) m = absmax8(x[i], m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -186,24 +195,40 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return b;
 }
 
-// q = e4m3(x / scale) with scale = amax / 448 (double, rounded to fp32; 1 if
-// amax == 0); block 0 stores the scale next to the amax.
+// Eight bf16 values times inv to eight E4M3 bytes.
+__device__ __forceinline__ uint2 quant8(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t b[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    b[k] = e4m3x2(__fmul_rn(bf16_bits_to_float(w[k] & 0xFFFFu), inv),
+                  __fmul_rn(bf16_bits_to_float(w[k] >> 16), inv));
+  return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+// q = e4m3(x * inv) with inv = 448 / amax (double, rounded to fp32 and capped at the
+// largest finite fp32, which only an amax below about 1.3e-36 reaches; 1 if
+// amax == 0); block 0 stores scale = amax / 448 (double, rounded to fp32; 1 if
+// amax == 0) next to the amax. One multiply per element instead of an IEEE divide.
 __global__ void quantize_e4m3_kernel(const uint4* __restrict__ x, int64_t n8, uint2* __restrict__ q,
                                      float* out) {
   const float amax = __ldcg(out + 1);
-  const float scale = amax > 0.f ? static_cast<float>(static_cast<double>(amax) / 448.0) : 1.f;
-  if (blockIdx.x == 0 && threadIdx.x == 0) out[0] = scale;
+  const float inv = amax > 0.f ? static_cast<float>(fmin(448.0 / static_cast<double>(amax),
+                                                         3.4028234663852886e38))
+                               : 1.f;
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    out[0] = amax > 0.f ? static_cast<float>(static_cast<double>(amax) / 448.0) : 1.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const uint4 v = x[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t b[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      b[k] = e4m3x2(__fdiv_rn(bf16_bits_to_float(w[k] & 0xFFFFu), scale),
-                    __fdiv_rn(bf16_bits_to_float(w[k] >> 16), scale));
-    q[i] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = __ldcs(x + i), b = __ldcs(x + i + stride), c = __ldcs(x + i + 2 * stride),
+                d = __ldcs(x + i + 3 * stride);
+    q[i] = quant8(a, inv);
+    q[i + stride] = quant8(b, inv);
+    q[i + 2 * stride] = quant8(c, inv);
+    q[i + 3 * stride] = quant8(d, inv);
   }
+  for (; i < n8; i += stride) q[i] = quant8(__ldcs(x + i), inv);
 }
 
 }  // namespace

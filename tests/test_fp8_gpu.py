@@ -73,12 +73,15 @@ def test_fp8_token_blocks_and_chunks(opts):
 
 def _quantize_expected(bits):
     """Per-tensor E4M3 quantisation as flce_quantize_e4m3 states it: scale = amax / 448
-    rounded to fp32 (1 for an all-zero tensor), the quotient x / scale in fp32, then
-    the nearest E4M3 code (flce_inputs.e4m3_encode)."""
+    and inv = 448 / amax rounded to fp32 (inv capped at the largest finite fp32; both 1
+    for an all-zero tensor), the product x * inv in fp32, then the nearest E4M3 code
+    (flce_inputs.e4m3_encode)."""
     x = flce_inputs.bf16_bits_to_f32(bits).astype(np.float32)
     amax = np.float32(np.max(np.abs(x)))
     scale = np.float32(float(amax) / 448.0) if amax > 0 else np.float32(1.0)
-    y = (x / scale).astype(np.float32)
+    big = float(np.finfo(np.float32).max)
+    inv = np.float32(min(448.0 / float(amax), big)) if amax > 0 else np.float32(1.0)
+    y = (x * inv).astype(np.float32)
     return flce_inputs.e4m3_encode(y.astype(np.float64)), scale, amax
 
 
@@ -90,7 +93,7 @@ def _wide_range_bf16(shape, seed):
     return flce_inputs.f32_to_bf16_bits(x.astype(np.float32))
 
 
-@pytest.mark.parametrize("case", ["normal", "wide", "zeros", "tiny", "ragged_grid"])
+@pytest.mark.parametrize("case", ["normal", "wide", "zeros", "tiny", "ragged_grid", "subnormal"])
 def test_device_quantizer_matches_its_definition(case):
     if case == "normal":
         bits = flce_inputs.normal_bf16((300, 256), 0.05, seed=3, stream=0)
@@ -101,6 +104,9 @@ def test_device_quantizer_matches_its_definition(case):
         bits[3, 5] = 0x8000  # -0 counts as zero
     elif case == "tiny":
         bits = flce_inputs.normal_bf16((1, 8), 1.0, seed=5, stream=0)
+    elif case == "subnormal":  # amax ~1e-39: 448 / amax overflows fp32, inv is capped
+        x = np.random.default_rng(7).uniform(-1, 1, (64, 40)).astype(np.float32) * np.float32(1e-39)
+        bits = flce_inputs.f32_to_bf16_bits(x)
     else:  # more 8-element groups than one grid pass covers
         bits = _wide_range_bf16((4099, 2056), seed=6)
     q_ref, scale_ref, amax_ref = _quantize_expected(bits)
