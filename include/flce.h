@@ -196,6 +196,44 @@ int flce_forward_backward_fp8(const uint8_t* H8, const float* scale_h, const uin
                               size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * Vocabulary shards: the local half of a vocabulary-parallel split (the lecture
+ * notes' open question on vocabularies above a million ids, where the chunks grow
+ * too large and the vocabulary has to be split). A device holding rows [v_offset, v_offset + V_shard) of W, as W_shard
+ * ([V_shard, D] bf16, its row 0 being row v_offset of W), runs the two calls
+ * below; the caller's collective combines the shards between them. labels hold
+ * ids of the whole vocabulary [0, V_total) (or ignore_index) and are the same on
+ * every shard; 0 <= v_offset, v_offset + V_shard <= V_total <= 2^30.
+ *
+ * flce_forward_shard writes, per token i (fp32 [N] each, 4-byte aligned):
+ *   m[i]  = max over the shard's ids v of z_iv
+ *   s[i]  = sum over the shard's ids v of exp(z_iv - m[i])
+ *   zt[i] = z_{i,y_i} when y_i lies in the shard, else 0 (also 0 for ignored tokens)
+ * The shards combine as  M_i = max_r m_r[i],  lse_i = M_i + log sum_r s_r[i] exp(m_r[i] - M_i),
+ * z_t,i = sum_r zt_r[i]  (an all-reduce with max, then sums), and
+ * loss = sum over non-ignored i of (lse_i - z_t,i) / n (sum: without the / n).
+ *
+ * flce_backward_shard takes that lse (fp32 [N], 4-byte aligned) and writes the
+ * shard's part of the gradients, G_iv = (exp(z_iv - lse_i) - [v = y_i]) * scale
+ * over the shard's ids (scale = grad_scale / n as in flce_forward_backward, n
+ * counted from the labels, or the normalizer option):
+ *   dH_part  fp32 [N, D], 16-byte aligned: G W_shard; the caller sums the parts of
+ *            all shards (then rounds to bf16 if it wants bf16 dH); nullable
+ *   dW_shard [V_shard, D], fp32 or bf16 (dw_dtype): the shard's rows of dW; nullable
+ * (not both null). Workspace: flce_workspace_size(N, D, V_shard, opt). Errors as in
+ * flce_forward_backward, plus FLCE_ERR_SHAPE for a shard outside [0, V_total) and
+ * FLCE_ERR_NULL for a missing m, s, zt or lse; a label outside [0, V_total) sets
+ * FLCE_ERR_LABEL_RANGE in *status.
+ */
+int flce_forward_shard(const uint16_t* H, const uint16_t* W_shard, const int32_t* labels,
+                       int64_t N, int64_t D, int64_t V_shard, int64_t v_offset, int64_t V_total,
+                       const flce_options* opt, float* m, float* s, float* zt, void* workspace,
+                       size_t ws_bytes, int32_t* status, void* stream);
+int flce_backward_shard(const uint16_t* H, const uint16_t* W_shard, const int32_t* labels,
+                        int64_t N, int64_t D, int64_t V_shard, int64_t v_offset, int64_t V_total,
+                        const flce_options* opt, const float* lse, float* dH_part, void* dW_shard,
+                        void* workspace, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * Per-tensor E4M3 quantisation on the device: the operand preparation the FP8
  * variant expects (the reading of the lecture notes' FP8 question that the FP8
  * entry points follow). Over the bf16 tensor x [n]:

@@ -8,15 +8,17 @@ device memory. The C ABI is include/flce.h; this package is its Python binding.
 from ._binding import (FLCE_ERR_ALIGN, FLCE_ERR_CUDA, FLCE_ERR_DEVICE, FLCE_ERR_LABEL_RANGE,
                        FLCE_ERR_NULL, FLCE_ERR_OPTION, FLCE_ERR_SHAPE, FLCE_ERR_TIMEOUT,
                        FLCE_ERR_WORKSPACE, FLCE_OK, FLCEError, LIB_PATH, Options, Result,
-                       ce_logits, check_status, forward, forward_backward, forward_backward_fp8, get_plan, lib, make_options, quantize_e4m3,
-                       scale_grads, status_string, workspace_size)
+                       ShardForward, backward_shard, ce_logits, check_status, forward,
+                       forward_backward, forward_backward_fp8, forward_shard, get_plan, lib,
+                       make_options, quantize_e4m3, scale_grads, status_string, workspace_size)
 from .loss import (FusedLinearCrossEntropyFunction, FusedLinearCrossEntropyLoss,
                    fused_linear_cross_entropy)
 
 __all__ = ["FLCE_ERR_ALIGN", "FLCE_ERR_CUDA", "FLCE_ERR_DEVICE", "FLCE_ERR_LABEL_RANGE",
            "FLCE_ERR_NULL", "FLCE_ERR_OPTION", "FLCE_ERR_SHAPE", "FLCE_ERR_TIMEOUT",
            "FLCE_ERR_WORKSPACE", "FLCE_OK", "FLCEError", "LIB_PATH", "Options", "Result",
-           "ce_logits", "check_status", "forward", "forward_backward", "forward_backward_fp8", "get_plan", "lib", "make_options", "quantize_e4m3",
-           "scale_grads", "status_string", "workspace_size",
+           "ShardForward", "backward_shard", "ce_logits", "check_status", "forward",
+           "forward_backward", "forward_backward_fp8", "forward_shard", "get_plan", "lib",
+           "make_options", "quantize_e4m3", "scale_grads", "status_string", "workspace_size",
            "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
            "fused_linear_cross_entropy"]

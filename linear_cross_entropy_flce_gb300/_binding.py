@@ -98,6 +98,14 @@ lib.flce_forward_backward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i6
 lib.flce_forward_backward_fp8.restype = ctypes.c_int
 lib.flce_scale_grads.argtypes = [_vp, _i64, _vp, _i64, ctypes.c_int32, _vp, _vp]
 lib.flce_scale_grads.restype = ctypes.c_int
+lib.flce_forward_shard.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                   ctypes.POINTER(Options), _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                   _vp, _vp]
+lib.flce_forward_shard.restype = ctypes.c_int
+lib.flce_backward_shard.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                    ctypes.POINTER(Options), _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                    _vp, _vp]
+lib.flce_backward_shard.restype = ctypes.c_int
 lib.flce_quantize_e4m3.argtypes = [_vp, _i64, _vp, _vp, _vp]
 lib.flce_quantize_e4m3.restype = ctypes.c_int
 lib.flce_check_status.argtypes = [_vp, _vp]
@@ -268,6 +276,77 @@ def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_forward")
     return Result(loss, lse, None, None, status)
+
+
+@dataclasses.dataclass
+class ShardForward:
+    m: object        # fp32 [N]: max over the shard's ids of z_iv
+    s: object        # fp32 [N]: sum over the shard's ids of exp(z_iv - m_i)
+    zt: object       # fp32 [N]: target logit if the label lies in the shard, else 0
+    status: object
+
+
+def forward_shard(H, W_shard, labels, v_offset: int, V_total: int, *, out: Optional[dict] = None,
+                  workspace=None, status=None, stream=None, **options) -> ShardForward:
+    """flce_forward_shard: the per-token (m, s, zt) of vocabulary rows
+    [v_offset, v_offset + len(W_shard)) of a V_total-id vocabulary (labels are
+    ids of the whole vocabulary)."""
+    import torch
+    N, D, V = _check_inputs(H, W_shard, labels)
+    opts = make_options(**options)
+    dev = H.device
+    out = dict(out or {})
+    m, s_, zt = (out.get(k) if out.get(k) is not None else
+                 torch.empty(N, dtype=torch.float32, device=dev) for k in ("m", "s", "zt"))
+    if workspace is None:
+        workspace = torch.empty(workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_forward_shard(_ptr(H), _ptr(W_shard), _ptr(labels), N, D, V, int(v_offset),
+                                int(V_total), ctypes.byref(opts), _ptr(m), _ptr(s_), _ptr(zt),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_shard")
+    return ShardForward(m, s_, zt, status)
+
+
+def backward_shard(H, W_shard, labels, lse, v_offset: int, V_total: int, *, need_dh: bool = True,
+                   need_dw: bool = True, out: Optional[dict] = None, workspace=None, status=None,
+                   stream=None, **options) -> Result:
+    """flce_backward_shard: from the combined lse, the shard's fp32 part of dH
+    (summed over the shards by the caller) and its rows of dW. Returns a Result
+    whose loss is None and whose dH is the fp32 part."""
+    import torch
+    N, D, V = _check_inputs(H, W_shard, labels)
+    if not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous() and lse.numel() == N):
+        raise ValueError("lse must be a contiguous CUDA float32 tensor of N values")
+    opts = make_options(**options)
+    dev = H.device
+    out = dict(out or {})
+    dH = out.get("dH")
+    if dH is None and need_dh:
+        dH = torch.empty(N, D, dtype=torch.float32, device=dev)
+    dW = out.get("dW")
+    if dW is None and need_dw:
+        dt = torch.float32 if options.get("dw_dtype", "float32") == "float32" else torch.bfloat16
+        dW = torch.empty(V, D, dtype=dt, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_backward_shard(_ptr(H), _ptr(W_shard), _ptr(labels), N, D, V, int(v_offset),
+                                 int(V_total), ctypes.byref(opts), _ptr(lse),
+                                 _ptr(dH) if need_dh else None, _ptr(dW) if need_dw else None,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_backward_shard")
+    return Result(None, lse, dH if need_dh else None, dW if need_dw else None, status)
 
 
 def ce_logits(logits, labels, *, need_grad: bool = True, in_place: bool = False,

@@ -287,6 +287,20 @@ struct Fp8Operands {
   const float* scale_w = nullptr;
 };
 
+// A call on one vocabulary shard, rows [v_offset, v_offset + V) of a vocabulary of
+// V_total ids (V_total == 0: an ordinary call over the whole vocabulary). The
+// forward writes the shard's per-token (m, s, zt); the backward takes the combined
+// lse and writes the shard's fp32 part of dH and its rows of dW.
+struct Shard {
+  int64_t v_offset = 0;
+  int64_t V_total = 0;
+  float* m = nullptr;
+  float* s = nullptr;
+  float* zt = nullptr;
+  const float* lse_in = nullptr;
+  float* dh_f32 = nullptr;
+};
+
 // uint8 matrix [outer][inner] read in boxes of box_inner x box_outer bytes with
 // 128-byte swizzle; out-of-range elements read as zero.
 bool encode_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
@@ -306,7 +320,7 @@ bool encode_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32_t* labels,
         int64_t N, int64_t D, int64_t V, const flce_options* opt_in, float* loss, float* lse_out,
         uint16_t* dH, void* dW, bool backward, void* workspace, size_t ws_bytes, int32_t* status,
-        void* stream_v) {
+        void* stream_v, const Shard& sh = Shard{}) {
   flce_options o;
   flce_default_options(&o);
   if (opt_in != nullptr) o = *opt_in;
@@ -315,8 +329,25 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
     dH = nullptr;
     dW = nullptr;
   }
-  const bool need_bf16 = !fp8 || dH != nullptr || dW != nullptr;
-  if (labels == nullptr || loss == nullptr || workspace == nullptr) return FLCE_ERR_NULL;
+  const bool shard = sh.V_total > 0;
+  // the backward of a shard writes fp32 dH parts instead of bf16 dH
+  const bool want_dh = dH != nullptr || (shard && backward && sh.dh_f32 != nullptr);
+  const bool need_bf16 = !fp8 || want_dh || dW != nullptr;
+  if (labels == nullptr || (!shard && loss == nullptr) || workspace == nullptr)
+    return FLCE_ERR_NULL;
+  if (shard) {
+    if (backward ? (sh.lse_in == nullptr || (!want_dh && dW == nullptr))
+                 : (sh.m == nullptr || sh.s == nullptr || sh.zt == nullptr))
+      return FLCE_ERR_NULL;
+    if (sh.v_offset < 0 || sh.V_total > (int64_t(1) << 30) || sh.v_offset + V > sh.V_total)
+      return FLCE_ERR_SHAPE;
+    const uintptr_t a4 = reinterpret_cast<uintptr_t>(sh.m) | reinterpret_cast<uintptr_t>(sh.s) |
+                         reinterpret_cast<uintptr_t>(sh.zt) | reinterpret_cast<uintptr_t>(sh.lse_in);
+    if ((a4 & 3u) || (sh.dh_f32 && !aligned16(sh.dh_f32))) return FLCE_ERR_ALIGN;
+  }
+  // labels are ids of the whole vocabulary
+  const int64_t V_lab = shard ? sh.V_total : V;
+  const int64_t v_base = shard ? sh.v_offset : 0;   // id of W's row 0
   if (fp8 && (f8.H8 == nullptr || f8.W8 == nullptr)) return FLCE_ERR_NULL;
   if (need_bf16 && (H == nullptr || W == nullptr)) return FLCE_ERR_NULL;
   int rc = check_shape(N, D, V);
@@ -351,7 +382,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   float* zt = reinterpret_cast<float*>(ws + P.off_zt);
   // reduction "none": the merge writes each token's loss straight to the caller
   float* nll = per_token ? loss : reinterpret_cast<float*>(ws + P.off_nll);
-  float* loss_scalar = per_token ? reinterpret_cast<float*>(ws + P.off_scal + 8) : loss;
+  float* loss_scalar =
+      (per_token || shard) ? reinterpret_cast<float*>(ws + P.off_scal + 8) : loss;
   float* lse = lse_out ? lse_out : reinterpret_cast<float*>(ws + P.off_lse);
   float* scal = reinterpret_cast<float*>(ws + P.off_scal);  // [0] scale
   int32_t* nvalid = reinterpret_cast<int32_t*>(ws + P.off_scal + 4);
@@ -390,47 +422,55 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   const uint32_t idesc_z = fp8 ? make_idesc_e4m3_f32(P.tile_m, BN) : make_idesc_bf16_f32(P.tile_m, BN, 0, 0);
 
 
-  // ---- 1. forward LSE GEMM ----
-  GemmParams g{};
-  g.a_mn_major = 0;
-  g.b_mn_major = 0;
-  g.m_blocks = P.m_blocks;
-  g.n_blocks = P.v_tiles;
-  g.k_blocks = k_blocks_z;
-  g.acc_scale_h = f8.scale_h;
-  g.acc_scale_w = f8.scale_w;
-  g.splits = P.splits;
-  g.part_stride = P.part_stride;
-  g.num_units = P.splits * P.m_blocks;
-  g.group_m = std::min(P.m_blocks, 16);
-  g.idesc = idesc_z;
-  g.timeout_ns = tmo;
-  g.status = status;
-  g.m_valid = static_cast<int>(N);
-  g.n_valid = static_cast<int>(V);
-  g.labels = labels;
-  g.row_base = 0;
-  g.col_base = 0;
-  g.ignore_index = o.ignore_index;
-  g.part = part;
-  g.zt = zt;
-  if (launch_gemm_lse(cta, mH_k, mW_k, g, cta * std::min(g.num_units, pairs), st, fp8 ? 1 : 0) !=
-          cudaSuccess ||
-      !trace())
-    return FLCE_ERR_CUDA;
+  // ---- 1. forward LSE GEMM (the backward of a shard starts from the given lse) ----
+  if (!(shard && backward)) {
+    GemmParams g{};
+    g.a_mn_major = 0;
+    g.b_mn_major = 0;
+    g.m_blocks = P.m_blocks;
+    g.n_blocks = P.v_tiles;
+    g.k_blocks = k_blocks_z;
+    g.acc_scale_h = f8.scale_h;
+    g.acc_scale_w = f8.scale_w;
+    g.splits = P.splits;
+    g.part_stride = P.part_stride;
+    g.num_units = P.splits * P.m_blocks;
+    g.group_m = std::min(P.m_blocks, 16);
+    g.idesc = idesc_z;
+    g.timeout_ns = tmo;
+    g.status = status;
+    g.m_valid = static_cast<int>(N);
+    g.n_valid = static_cast<int>(V);
+    g.labels = labels;
+    g.row_base = 0;
+    g.col_base = static_cast<int>(v_base);
+    g.ignore_index = o.ignore_index;
+    g.part = part;
+    g.zt = zt;
+    if (launch_gemm_lse(cta, mH_k, mW_k, g, cta * std::min(g.num_units, pairs), st, fp8 ? 1 : 0) !=
+            cudaSuccess ||
+        !trace())
+      return FLCE_ERR_CUDA;
 
-  // ---- 2./3. merge and reduce ----
-  if (launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V), P.part_stride,
-                       P.splits, o.ignore_index, lse, nll, st) != cudaSuccess ||
-      !trace())
-    return FLCE_ERR_CUDA;
-  if (launch_loss_reduce(nll, labels, static_cast<int>(N), static_cast<int>(V), o.ignore_index,
+    // ---- 2. merge: lse and NLL, or a shard's (m, s, zt) ----
+    const cudaError_t me =
+        shard ? launch_shard_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(v_base),
+                                   static_cast<int>(v_base + V), P.part_stride, P.splits,
+                                   o.ignore_index, sh.m, sh.s, sh.zt, st)
+              : launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V),
+                                 P.part_stride, P.splits, o.ignore_index, lse, nll, st);
+    if (me != cudaSuccess || !trace()) return FLCE_ERR_CUDA;
+  }
+  // ---- 3. reduce: label check, n, the gradient scale and (not for shards) the loss ----
+  if (launch_loss_reduce(shard ? nullptr : nll, labels, static_cast<int>(N),
+                         static_cast<int>(V_lab), o.ignore_index,
                          per_token ? FLCE_REDUCTION_SUM : o.reduction, o.grad_scale,
                          o.normalizer, loss_scalar, scal, nvalid, status,
                          st) != cudaSuccess ||
       !trace())
     return FLCE_ERR_CUDA;
-  if (dH == nullptr && dW == nullptr) return FLCE_OK;
+  if (!want_dh && dW == nullptr) return FLCE_OK;
+  const float* lse_g = shard ? sh.lse_in : lse;   // the lse the gradient is formed from
 
   // ---- 4. backward, token block outer, vocabulary chunk inner ----
   const int64_t rows_b = ceil_div(P.n_block, P.tile_m) * P.tile_m;
@@ -479,9 +519,9 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
       q.n_valid = c_len;
       q.labels = labels;
       q.row_base = static_cast<int>(b0);
-      q.col_base = static_cast<int>(c0);
+      q.col_base = static_cast<int>(v_base + c0);
       q.ignore_index = o.ignore_index;
-      q.lse = lse;
+      q.lse = lse_g;
       q.scale = scal;
       q.out_row0 = 0;
       if (launch_gemm_grad(cta, mH_k, mW_k, mG_out, q, cta * std::min(q.num_units, pairs), st,
@@ -527,7 +567,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
           return FLCE_ERR_CUDA;
       }
 
-      if (dH != nullptr) {
+      if (want_dh) {
         // dH rows [b0, b0 + nb_len) (+)= G_bc W_c: M = tokens, N = hidden, K = vocabulary.
         GemmParams h{};
         h.a_mn_major = 0;
@@ -549,11 +589,13 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         // one chunk: bf16 dH directly; else an fp32 accumulator of this token
         // block's rows (stored by chunk 0, reduce-added by the others), rounded
         // to bf16 after the last chunk. The map holds exactly the block's rows.
+        // A shard accumulates straight into its fp32 dH part.
         CUtensorMap mDH;
-        const bool dh_direct = P.n_chunks == 1;
-        if (!(dh_direct ? encode_out(&mDH, dH + b0 * D, true, D, nb_len, D)
-                        : encode_out(&mDH, dh_acc, false, D, nb_len, D)))
-          return FLCE_ERR_CUDA;
+        const bool dh_direct = P.n_chunks == 1 && !shard;
+        const bool ok_dh = shard ? encode_out(&mDH, sh.dh_f32 + b0 * D, false, D, nb_len, D)
+                           : dh_direct ? encode_out(&mDH, dH + b0 * D, true, D, nb_len, D)
+                                       : encode_out(&mDH, dh_acc, false, D, nb_len, D);
+        if (!ok_dh) return FLCE_ERR_CUDA;
         h.out_row0 = 0;
         h.out_mode = dh_direct ? OUT_STORE_BF16 : (c == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
         if (launch_gemm_f32(cta, mG_k, mW_mn, mDH, h, cta * std::min(h.num_units, pairs), st) !=
@@ -562,7 +604,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
           return FLCE_ERR_CUDA;
       }
     }
-    if (dH != nullptr && P.n_chunks > 1 &&
+    if (dH != nullptr && !shard && P.n_chunks > 1 &&
         (launch_f32_to_bf16(dh_acc, dH + b0 * D, static_cast<int64_t>(nb_len) * D, sms, st) !=
              cudaSuccess ||
          !trace()))
@@ -746,6 +788,35 @@ int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, in
                  size_t ws_bytes, int32_t* status, void* stream) {
   return flce::run(H, W, flce::Fp8Operands{}, labels, N, D, V, opt, loss, lse, nullptr, nullptr,
                    false, workspace, ws_bytes, status, stream);
+}
+
+int flce_forward_shard(const uint16_t* H, const uint16_t* W_shard, const int32_t* labels,
+                       int64_t N, int64_t D, int64_t V_shard, int64_t v_offset, int64_t V_total,
+                       const flce_options* opt, float* m, float* s, float* zt, void* workspace,
+                       size_t ws_bytes, int32_t* status, void* stream) {
+  if (V_total < 1) return FLCE_ERR_SHAPE;
+  flce::Shard sh;
+  sh.v_offset = v_offset;
+  sh.V_total = V_total;
+  sh.m = m;
+  sh.s = s;
+  sh.zt = zt;
+  return flce::run(H, W_shard, flce::Fp8Operands{}, labels, N, D, V_shard, opt, nullptr, nullptr,
+                   nullptr, nullptr, false, workspace, ws_bytes, status, stream, sh);
+}
+
+int flce_backward_shard(const uint16_t* H, const uint16_t* W_shard, const int32_t* labels,
+                        int64_t N, int64_t D, int64_t V_shard, int64_t v_offset, int64_t V_total,
+                        const flce_options* opt, const float* lse, float* dH_part, void* dW_shard,
+                        void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  if (V_total < 1) return FLCE_ERR_SHAPE;
+  flce::Shard sh;
+  sh.v_offset = v_offset;
+  sh.V_total = V_total;
+  sh.lse_in = lse;
+  sh.dh_f32 = dH_part;
+  return flce::run(H, W_shard, flce::Fp8Operands{}, labels, N, D, V_shard, opt, nullptr, nullptr,
+                   nullptr, dW_shard, true, workspace, ws_bytes, status, stream, sh);
 }
 
 int flce_forward_fp8(const uint8_t* H8, const float* scale_h, const uint8_t* W8,

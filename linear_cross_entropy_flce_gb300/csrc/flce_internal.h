@@ -33,7 +33,14 @@ cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t*
                              int V, int part_stride, int splits, int ignore_index, float* lse,
                              float* nll, cudaStream_t stream);
 
-// One-block deterministic reduction: label validation, n_valid, the loss and
+// Vocabulary shard [v_lo, v_hi): per token the shard's max m, sum of exp(z - m)
+// and the target logit when the label lies in the shard (else 0).
+cudaError_t launch_shard_merge(const float2* part, const float* zt, const int32_t* labels, int N,
+                               int v_lo, int v_hi, int part_stride, int splits, int ignore_index,
+                               float* m, float* s, float* zt_out, cudaStream_t stream);
+
+// One-block deterministic reduction: label validation, n_valid, the loss (nll may
+// be null: the loss is then 0 and only n, the scale and the label check count) and
 // the gradient scale grad_scale / n (or / normalizer, or 1 for "sum").
 cudaError_t launch_loss_reduce(const float* nll, const int32_t* labels, int N, int V,
                                int ignore_index, int reduction, float grad_scale,

@@ -41,6 +41,31 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   nll[i] = (y != ignore_index && y >= 0 && y < V) ? L - zt[i] : 0.f;
 }
 
+// One vocabulary shard (ids [v_lo, v_hi) of a vocabulary split over several
+// calls): the per-token merge of the shard's vocabulary-range partials into its
+// (max, sum of exponentials), and the target logit when the token's label lies
+// in the shard (else 0), so that the shards combine by max, rescaled sum and sum.
+__global__ void shard_merge_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
+                                   const int32_t* __restrict__ labels, int N, int v_lo, int v_hi,
+                                   int part_stride, int splits, int ignore_index,
+                                   float* __restrict__ m_out, float* __restrict__ s_out,
+                                   float* __restrict__ zt_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int r = i / BM, l = i - (i / BM) * BM;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[(static_cast<int64_t>(s) * part_stride + r) * BM + l].x);
+  float S = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float2 pr = part[(static_cast<int64_t>(s) * part_stride + r) * BM + l];
+    S += pr.y * ex2f_approx((pr.x - M) * kLog2e);
+  }
+  m_out[i] = M;
+  s_out[i] = S;
+  const int y = labels[i];
+  zt_out[i] = (y != ignore_index && y >= v_lo && y < v_hi) ? zt[i] : 0.f;
+}
+
 constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -61,7 +86,7 @@ __global__ void __launch_bounds__(kReduceThreads)
       continue;
     }
     ++cnt;
-    acc += static_cast<double>(nll[i]);
+    if (nll != nullptr) acc += static_cast<double>(nll[i]);
   }
   s_sum[t] = acc;
   s_cnt[t] = cnt;
@@ -282,6 +307,15 @@ cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t*
   const int threads = 256;
   lse_merge_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(
       part, zt, labels, N, V, part_stride, splits, ignore_index, lse, nll);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_merge(const float2* part, const float* zt, const int32_t* labels, int N,
+                               int v_lo, int v_hi, int part_stride, int splits, int ignore_index,
+                               float* m, float* s, float* zt_out, cudaStream_t stream) {
+  const int threads = 256;
+  shard_merge_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(
+      part, zt, labels, N, v_lo, v_hi, part_stride, splits, ignore_index, m, s, zt_out);
   return cudaGetLastError();
 }
 

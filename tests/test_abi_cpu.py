@@ -25,6 +25,7 @@ def test_header_declares_the_abi():
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
                             "flce_ce_workspace_size", "flce_ce_logits", "flce_forward_fp8",
                             "flce_forward_backward_fp8", "flce_quantize_e4m3",
+                            "flce_forward_shard", "flce_backward_shard",
                             "flce_scale_grads",
                             "flce_check_status", "flce_status_string"])
 
@@ -161,6 +162,34 @@ def test_fp8_host_rejections():
     # the gradient products need the bf16 operands
     assert g(0x1000, 0x8000, 0x2000, 0x8004, None, None, 0x3000, 64, 128, 1000, None, 0x4000,
              None, 0x6000, 0x7000, 0x5000, 1 << 30, None, None) == flce.FLCE_ERR_NULL
+
+
+def test_shard_host_rejections():
+    f = flce.lib.flce_forward_shard
+    ok = dict(H=0x1000, W=0x2000, y=0x3000, N=64, D=128, V=500, off=500, Vt=1000, m=0x4000,
+              s=0x5000, zt=0x6000, ws=0x7000)
+
+    def fwd(**kw):
+        a = dict(ok, **kw)
+        return f(a["H"], a["W"], a["y"], a["N"], a["D"], a["V"], a["off"], a["Vt"], None, a["m"],
+                 a["s"], a["zt"], a["ws"], 1 << 30, None, None)
+
+    assert fwd(m=None) == flce.FLCE_ERR_NULL
+    assert fwd(zt=None) == flce.FLCE_ERR_NULL
+    assert fwd(off=-1) == flce.FLCE_ERR_SHAPE
+    assert fwd(off=501) == flce.FLCE_ERR_SHAPE     # past the whole vocabulary
+    assert fwd(Vt=0) == flce.FLCE_ERR_SHAPE
+    assert fwd(s=0x5002) == flce.FLCE_ERR_ALIGN
+    g = flce.lib.flce_backward_shard
+
+    def bwd(lse=0x8000, dh=0x9000, dw=0xA000, off=500):
+        return g(0x1000, 0x2000, 0x3000, 64, 128, 500, off, 1000, None, lse, dh, dw, 0x7000,
+                 1 << 30, None, None)
+
+    assert bwd(lse=None) == flce.FLCE_ERR_NULL
+    assert bwd(dh=None, dw=None) == flce.FLCE_ERR_NULL
+    assert bwd(dh=0x9008) == flce.FLCE_ERR_ALIGN   # TMA base of the fp32 dH part
+    assert bwd(off=600) == flce.FLCE_ERR_SHAPE
 
 
 def test_quantize_e4m3_host_rejections():
