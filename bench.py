@@ -460,6 +460,7 @@ def main(argv=None) -> int:
     torch.cuda.synchronize(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]   # cross-check through cudaMemGetInfo
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def call(**kw):
@@ -488,21 +489,34 @@ def main(argv=None) -> int:
     if code != flce.FLCE_OK:
         raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
     peak_delta = torch.cuda.max_memory_allocated(dev) - base
+    torch.cuda.synchronize(dev)
+    # device memory that left the free pool over the workspace allocation and the
+    # warm-up calls (the allocator's 2 MB segment rounding and the first launch's
+    # module loading included)
+    free_delta = free0 - torch.cuda.mem_get_info(dev)[0]
 
     # ---- device-timed steps (inputs resident) ----
+    # an event between consecutive steps (recorded on the same stream, no
+    # synchronisation) gives each step's time for the median and the minimum
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps - 1)]
     with ClockSampler(local) as clk:
         rep.barrier()
         torch.cuda.synchronize(dev)
         ev0.record(stream)
-        for _ in range(args.steps):
+        for k in range(args.steps):
             step()
+            if k < args.steps - 1:
+                ev_step[k].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         rep.barrier()
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms = rep.max(ms_local)
+    bounds = [ev0] + ev_step + [ev1]
+    per_step = sorted(bounds[k].elapsed_time(bounds[k + 1]) for k in range(args.steps))
+    step_stats = {"median": per_step[len(per_step) // 2], "min": per_step[0], "max": per_step[-1]}
     code = flce.check_status(status, stream.cuda_stream)
     if code != flce.FLCE_OK:
         raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
@@ -668,8 +682,10 @@ def main(argv=None) -> int:
         "vs_baseline": None, "dtype": "e4m3 logits products + bf16 gradient products" if fp8 else "bf16", "data": "synthetic (seeded; no dataset or weights)",
         "config": config_block(wl, world),
         "tflops": tflops, "frac_bf16_peak": tflops / peak,
+        "ms_per_step_stats": step_stats,
         "peak_extra_hbm_bytes": int(peak_delta),
         "workspace_bytes": ws_bytes, "allocator_peak_delta_bytes": int(peak_delta),
+        "cuda_free_bytes_delta": int(free_delta),
         "logits_bytes_unfused": N * V * 4,
         "plan": plan,
         "gpu_launches": (plan["kernel_launches"] + (4 if fp8 is not None else 0)) * args.steps,
