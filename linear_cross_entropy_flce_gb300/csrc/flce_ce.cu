@@ -33,6 +33,7 @@ namespace flce {
 namespace {
 
 constexpr int kCeThreads = 512;
+constexpr int kMaxCeCluster = 8;  // CTAs per row at most (portable cluster size)
 constexpr int kCountThreads = 1024;
 
 __device__ __forceinline__ float ex2a(float x) {
@@ -147,6 +148,23 @@ __device__ __forceinline__ void cluster_barrier() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores v into `local`'s copy in CTA `rank` of the cluster and counts its 16
+// bytes on that CTA's mbarrier `bar_local` (the same offset in the peer): the
+// receiver learns of the data by waiting on its own barrier, with no fence over
+// this thread's other (global) stores.
+__device__ __forceinline__ void st_async_f4(const float4* local, uint64_t* bar_local, uint32_t rank,
+                                            float4 v) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(bar_local));
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(b), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+      : "memory");
 }
 
 __device__ __forceinline__ float2 ld_dsmem_f2(const float2* local, uint32_t rank) {
@@ -368,8 +386,12 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   constexpr int kElt = kBf16 ? 2 : 4;
   extern __shared__ __align__(128) uint8_t ce_smem[];
   __shared__ __align__(8) uint64_t s_bar[2];
+  // per-row exchange: every CTA of the cluster stores its (max, sum exp, target
+  // logit if the label is in its slice) into slot [row parity][its rank] of every
+  // CTA, counted on that CTA's s_xbar[row parity]
+  __shared__ __align__(8) uint64_t s_xbar[2];
+  __shared__ __align__(16) float4 s_msg[2][kMaxCeCluster];
   __shared__ float2 s_red[kCeThreads / 32];
-  __shared__ float2 s_part[2];
   __shared__ float s_lse;
   __shared__ int s_y;
   const int tid = threadIdx.x;
@@ -390,9 +412,12 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_xbar[0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_xbar[1])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  cluster_barrier();  // every CTA's exchange barriers exist before any peer stores to them
 
   // thread 0: expect the slice's bytes on the buffer's barrier and copy it
   auto issue = [&](int row, int b) {
@@ -507,32 +532,43 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
         const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
         lse_merge(m, s, m2, s2);
       }
-      if (lane == 0) s_part[it & 1] = make_float2(m, s);
-    }
-    // The target logit is read before the cluster barrier: after it, peers may
-    // overwrite their slices with the gradient (in place).
-    int y = -1;
-    bool valid = false;
-    float zt = 0.f;
-    if (tid == 0) {
-      y = labels[row];
-      valid = y != ignore_index && y >= 0 && y < V;
-      if (crank == 0 && valid) zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
-    }
-    cluster_barrier();
-    if (tid == 0) {
-      float M = -INFINITY, S = 0.f;
-      for (int r = 0; r < csize; ++r) {
-        const float2 pr = ld_dsmem_f2(&s_part[it & 1], static_cast<uint32_t>(r));
-        lse_merge(M, S, pr.x, pr.y);
+      if (lane == 0) {  // tid 0: send this CTA's part of the row to every CTA
+        const int y = labels[row];
+        const bool valid = y != ignore_index && y >= 0 && y < V;
+        // the target logit, from this CTA's staged slice (or its global tail),
+        // so that no CTA reads a part of the row a peer may be overwriting
+        float zt = 0.f;
+        if (valid && y >= v0 * E && y < v1 * E)
+          zt = kBf16 ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(
+                           sl + static_cast<int64_t>(y - v0 * E) * 2)) << 16)
+                     : *reinterpret_cast<const float*>(sl + static_cast<int64_t>(y - v0 * E) * 4);
+        else if (valid && last && y >= nvec * E)
+          zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
+        const int k = it & 1;
+        for (int r = 0; r < csize; ++r)
+          st_async_f4(&s_msg[k][crank], &s_xbar[k], static_cast<uint32_t>(r),
+                      make_float4(m, s, zt, 0.f));
+        const uint32_t xb = smem_addr(&s_xbar[k]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xb),
+                     "r"(static_cast<uint32_t>(16 * csize))
+                     : "memory");
+        if (!wait_phase_bounded(xb, static_cast<uint32_t>((it >> 1) & 1),
+                                static_cast<uint64_t>(timeout_ns)))
+          timed_out = true;
+        float M = -INFINITY, S = 0.f, ZT = 0.f;
+        for (int r = 0; r < csize; ++r) {
+          const float4 pr = s_msg[k][r];
+          lse_merge(M, S, pr.x, pr.y);
+          ZT += pr.z;
+        }
+        const float lse = M + logf(S);
+        if (crank == 0) {
+          if (lse_out != nullptr) lse_out[row] = lse;
+          nll_out[row] = valid ? lse - ZT : 0.f;
+        }
+        s_lse = lse;
+        s_y = valid ? y : -1;
       }
-      const float lse = M + logf(S);
-      if (crank == 0) {
-        if (lse_out != nullptr) lse_out[row] = lse;
-        nll_out[row] = valid ? lse - zt : 0.f;
-      }
-      s_lse = lse;
-      s_y = valid ? y : -1;
     }
     __syncthreads();
     if constexpr (kGrad) {
