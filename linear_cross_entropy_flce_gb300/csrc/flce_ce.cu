@@ -20,8 +20,11 @@
 //                     16-byte vector loads; the gradient pass re-reads its slice
 //                     (from L2 when the live rows fit in it).
 // Both merge per-thread running (max, sum exp) across the block and then across
-// the cluster through distributed shared memory, then form lse and the
-// per-token loss.
+// the cluster, then form lse and the per-token loss: the staged kernel by
+// asynchronous stores of each CTA's (max, sum exp, target logit) into every
+// CTA's shared memory, counted on the receiver's mbarrier (so the previous row's
+// gradient stores need not drain first); the streamed kernel through distributed
+// shared memory reads after one cluster barrier per row.
 // The loss itself is formed by loss_reduce_kernel (flce_reduce.cu).
 #include <cmath>
 #include <cstdint>
