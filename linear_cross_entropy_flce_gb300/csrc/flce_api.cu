@@ -14,6 +14,10 @@
 //        dH GEMM    dH_b  (+)= G_bc W_c     (fp32 accumulator; the last chunk
 //                   rounds to bf16)              (same page, 2.)
 // Nothing of size N x V is ever written: the largest buffer is one G chunk.
+// flce_forward runs steps 1-3. On one vocabulary shard, flce_forward_shard runs
+// step 1 with global label ids, a merge into the shard's (m, s, zt) and step 3
+// for the label check; flce_backward_shard runs step 3 for the scale and step 4
+// from the caller's combined lse, accumulating its dH part in fp32.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
