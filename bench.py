@@ -655,7 +655,7 @@ def main(argv=None) -> int:
     clocks = clk.summary()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # N = 1 only
         r = cpu_oracle_sample(wl, min(args.cpu_tokens, wl.N))
         cpu = {"value": r["tokens"] / r["seconds"], "unit": UNIT, "cores": blas_threads(),
                "kind": "oracle", "seconds": r["seconds"],
