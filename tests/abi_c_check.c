@@ -33,6 +33,26 @@ int main(void) {
   CHECK(flce_ce_workspace_size(8192, 128256, NULL, &bytes) == FLCE_OK && bytes > 0);
   CHECK(flce_forward_backward(NULL, NULL, NULL, 8, 64, 100, &o, NULL, NULL, NULL, NULL, NULL, 0,
                               NULL, NULL) == FLCE_ERR_NULL);
+  {
+    /* the shard, FP8 and quantiser entry points reject bad arguments on the host */
+    float m[4], s[4], zt[4];
+    CHECK(flce_forward_shard((const uint16_t*)0x1000, (const uint16_t*)0x2000,
+                             (const int32_t*)0x3000, 64, 128, 500, 501, 1000, &o, m, s, zt,
+                             (void*)0x7000, (size_t)1 << 30, NULL, NULL) == FLCE_ERR_SHAPE);
+    CHECK(flce_forward_shard((const uint16_t*)0x1000, (const uint16_t*)0x2000,
+                             (const int32_t*)0x3000, 64, 128, 500, 500, 1000, &o, NULL, s, zt,
+                             (void*)0x7000, (size_t)1 << 30, NULL, NULL) == FLCE_ERR_NULL);
+    CHECK(flce_backward_shard((const uint16_t*)0x1000, (const uint16_t*)0x2000,
+                              (const int32_t*)0x3000, 64, 128, 500, 500, 1000, &o, NULL,
+                              (float*)0x9000, NULL, (void*)0x7000, (size_t)1 << 30, NULL,
+                              NULL) == FLCE_ERR_NULL);
+    CHECK(flce_forward_fp8((const uint8_t*)0x1000, NULL, (const uint8_t*)0x2000,
+                           (const float*)0x8004, (const int32_t*)0x3000, 64, 128, 1000, &o,
+                           (float*)0x4000, NULL, (void*)0x5000, (size_t)1 << 30, NULL,
+                           NULL) == FLCE_ERR_NULL);
+    CHECK(flce_quantize_e4m3((const uint16_t*)0x1000, 12, (uint8_t*)0x2000, (float*)0x3000,
+                             NULL) == FLCE_ERR_ALIGN);
+  }
   CHECK(flce_status_string(FLCE_OK) != NULL && flce_status_string(FLCE_ERR_TIMEOUT) != NULL);
   CHECK(flce_status_string(12345) != NULL);
   printf("ok\n");
