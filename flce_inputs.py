@@ -3,7 +3,9 @@
 This module is shared by the CUDA path's tests and bench and by the CPU
 oracle's tests. It holds no arithmetic of the method itself: it only draws
 hidden states H, LM-head weights W and labels y, rounds the floating-point
-draws to bfloat16 bit patterns, and places ignored tokens.
+draws to bfloat16 bit patterns (and widens them back), and places ignored
+tokens. The FP8 variant's operand quantisation is part of what is checked, so
+its reference lives in the oracle (oracle/e4m3.py), not here.
 
 The workloads stand in for the language-model heads the Liger Kernel pages
 discuss ("Liger Kernel: Fused Triton Kernels for LLM Training", section
@@ -79,60 +81,6 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     """Exact widening of bfloat16 bit patterns to float64."""
     return bf16_bits_to_f32(b).astype(np.float64)
-
-
-# ---- FP8 (E4M3) operands --------------------------------------------------------
-# E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
-# codes 0x7F / 0xFF are NaN, largest finite 448, smallest subnormal 2^-9.
-
-def e4m3_table() -> np.ndarray:
-    """float64 value of each non-negative finite code 0x00..0x7E (index = code)."""
-    codes = np.arange(0x7F)
-    e = codes >> 3
-    m = codes & 7
-    return np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
-
-
-def e4m3_decode(bits: np.ndarray) -> np.ndarray:
-    """float64 values of E4M3 bytes (NaN codes decode to NaN)."""
-    b = np.asarray(bits, dtype=np.uint8)
-    mag = b & 0x7F
-    tab = np.append(e4m3_table(), np.nan)
-    v = tab[mag]
-    return np.where(b & 0x80, -v, v)
-
-
-def e4m3_encode(x: np.ndarray) -> np.ndarray:
-    """Round float values to the nearest E4M3 code (ties to the even code),
-    saturating at +-448. Returns uint8 codes."""
-    x = np.asarray(x, dtype=np.float64)
-    tab = e4m3_table()
-    a = np.minimum(np.abs(x), tab[-1])
-    hi = np.clip(np.searchsorted(tab, a, side="left"), 1, len(tab) - 1)
-    lo = hi - 1
-    dlo = a - tab[lo]
-    dhi = tab[hi] - a
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
-    code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    code = np.where(a == tab[hi], hi, code).astype(np.uint8)
-    return np.where(np.signbit(x) & (code != 0), code | 0x80, code).astype(np.uint8)
-
-
-def to_fp8_per_tensor(x_bf16_bits: np.ndarray, block_rows: int = 8192):
-    """Per-tensor amax scaling of a bf16 tensor into E4M3: scale = amax / 448 and
-    inv = 448 / amax, each rounded to float32 (inv capped at the largest finite
-    float32; both 1 for an all-zero tensor), and codes = e4m3(x * inv), the product
-    taken in float32. Returns (uint8 codes, float32 scale)."""
-    amax = 0.0
-    for r0 in range(0, x_bf16_bits.shape[0], block_rows):
-        amax = max(amax, float(np.max(np.abs(bf16_bits_to_f32(x_bf16_bits[r0:r0 + block_rows])))))
-    scale = np.float32(amax / 448.0 if amax > 0 else 1.0)
-    inv = np.float32(min(448.0 / amax, float(np.finfo(np.float32).max)) if amax > 0 else 1.0)
-    out = np.empty(x_bf16_bits.shape, dtype=np.uint8)
-    for r0 in range(0, x_bf16_bits.shape[0], block_rows):
-        blk = bf16_bits_to_f32(x_bf16_bits[r0:r0 + block_rows]).astype(np.float32)
-        out[r0:r0 + block_rows] = e4m3_encode((blk * inv).astype(np.float64))
-    return out, scale
 
 
 def normal_bf16(shape, scale: float, seed: int, stream: int, block_rows: int = 4096) -> np.ndarray:

@@ -83,7 +83,8 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
          grad_scale: float = 1.0, normalizer: float = 0.0,
          dh_rows: Optional[Sequence[int]] = None, dw_rows: Optional[Sequence[int]] = None,
          want_grads: bool = True, row_block: int = 512, vocab_block: int = 4096,
-         Hg: Optional[np.ndarray] = None, Wg: Optional[np.ndarray] = None) -> dict:
+         Hg: Optional[np.ndarray] = None, Wg: Optional[np.ndarray] = None,
+         want_abs: bool = False) -> dict:
     """Loss, per-token LSE and gradients of fused linear cross-entropy, float64.
 
     H: [N, D], W: [V, D] (any real dtype; values are taken exactly in float64),
@@ -96,8 +97,13 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
     dH = G Wg and dW = G^T Hg. The FP8 variant passes the dequantised FP8
     operands as H, W (they define the logits) and their bf16 originals as Hg, Wg. lse is always computed for every token because
     the loss and every dW row need all of them.
+    want_abs also returns the same two products taken over magnitudes,
+    dH_abs = |G| |Wg| and dW_abs = |G|^T |Hg| (rows as selected): the scale
+    against which the rounding of each gradient element is measured (an
+    element-wise error bound proportional to them holds even where the signed
+    sums cancel).
     Returns dict(loss, lse[N], nll[N] (0 on ignored tokens), n_valid, dH, dW,
-    dh_rows, dw_rows).
+    dh_rows, dw_rows, dH_abs, dW_abs).
     """
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -130,6 +136,7 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
     lse = np.empty(N, dtype=np.float64)
     nll = np.zeros(N, dtype=np.float64)
     dH = np.zeros((len(dh_sel), D), dtype=np.float64) if want_grads else None
+    dH_abs = np.zeros((len(dh_sel), D), dtype=np.float64) if (want_grads and want_abs) else None
     dh_pos = {int(r): k for k, r in enumerate(dh_sel)}
 
     # Pass over tokens: logits row, LSE, target logit, and dH for requested rows.
@@ -150,8 +157,11 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
                 G *= scale
                 G[~valid[sel]] = 0.0
                 out = G @ Wg
+                out_abs = np.abs(G) @ np.abs(Wg) if want_abs else None
                 for k, r in enumerate(sel):
                     dH[dh_pos[int(r)]] = out[k]
+                    if want_abs:
+                        dH_abs[dh_pos[int(r)]] = out_abs[k]
 
     loss_sum = math.fsum(nll[valid].tolist())
     if reduction == "sum":
@@ -162,10 +172,13 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
         loss = loss_sum / n_valid if n_valid > 0 else 0.0
 
     dW = None
+    dW_abs = None
     if want_grads:
         # Pass over vocabulary ids: the column block of G over all tokens, then
         # dW_v = sum_i g_iv h_i for every v in the block.
         dW = np.zeros((len(dw_sel), D), dtype=np.float64)
+        if want_abs:
+            dW_abs = np.zeros((len(dw_sel), D), dtype=np.float64)
         Hv = H[valid]
         Hgv = Hg[valid]
         yv = y[valid]
@@ -177,9 +190,11 @@ def flce(H: np.ndarray, W: np.ndarray, labels: np.ndarray, *,
             Gc -= (yv[:, None] == vids[None, :])
             Gc *= scale
             dW[c0:c0 + len(vids)] = Gc.T @ Hgv
+            if want_abs:
+                dW_abs[c0:c0 + len(vids)] = np.abs(Gc).T @ np.abs(Hgv)
 
     return dict(loss=loss, lse=lse, nll=nll, n_valid=n_valid, dH=dH, dW=dW,
-                dh_rows=dh_sel, dw_rows=dw_sel)
+                dh_rows=dh_sel, dw_rows=dw_sel, dH_abs=dH_abs, dW_abs=dW_abs)
 
 
 def ce_logits(Z: np.ndarray, labels: np.ndarray, *, ignore_index: int = IGNORE_INDEX,

@@ -15,7 +15,7 @@ import pytest
 
 import flce_inputs
 import oracle
-from flce_testlib import assert_within, compare, rel_fro, tensor_to_f64, to_device
+from flce_testlib import oracle_check, rel_fro, tensor_to_f64, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -63,8 +63,9 @@ def test_outputs_and_workspace_stay_inside_their_buffers(N, D, V, opts):
     assert flce.check_status(res.status) == flce.FLCE_OK
     for k, b in bufs.items():
         assert _guards_intact(b), k
-    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y)
-    assert_within(compare(res, ref))
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y,
+                      want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref, opts)
 
 
 def test_shift_of_every_weight_row_changes_only_lse():

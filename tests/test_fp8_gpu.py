@@ -6,7 +6,8 @@ import pytest
 
 import flce_inputs
 import oracle
-from flce_testlib import assert_within, compare, to_device
+from oracle import e4m3
+from flce_testlib import oracle_check, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -17,13 +18,14 @@ if torch.cuda.is_available():
 
 def _case(wl):
     Hb, Wb, y = flce_inputs.make_inputs(wl)
-    H8, sh = flce_inputs.to_fp8_per_tensor(Hb)
-    W8, sw = flce_inputs.to_fp8_per_tensor(Wb)
+    qh = e4m3.quantize_per_tensor(flce_inputs.bf16_bits_to_f32(Hb))
+    qw = e4m3.quantize_per_tensor(flce_inputs.bf16_bits_to_f32(Wb))
+    H8, sh, W8, sw = qh["codes"], qh["scale"], qw["codes"], qw["scale"]
     dev = torch.device("cuda:0")
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     H, W, lab = to_device(Hb, Wb, y)
-    He = flce_inputs.e4m3_decode(H8) * np.float64(sh)
-    We = flce_inputs.e4m3_decode(W8) * np.float64(sw)
+    He = e4m3.e4m3_decode(H8) * np.float64(sh)
+    We = e4m3.e4m3_decode(W8) * np.float64(sw)
     return (t(H8), float(sh), t(W8), float(sw), lab, H, W), (He, We, Hb, Wb, y)
 
 
@@ -35,10 +37,8 @@ def test_fp8_forward_backward_parity(shape):
     res = flce.forward_backward_fp8(H8, sh, W8, sw, lab, H, W)
     assert flce.check_status(res.status) == flce.FLCE_OK
     ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
-                      Wg=flce_inputs.bf16_bits_to_f64(Wb))
-    errs = compare(res, ref)
-    print(errs)
-    assert_within(errs)
+                      Wg=flce_inputs.bf16_bits_to_f64(Wb), want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref)
 
 
 def test_fp8_forward_only_and_llama2_workload():
@@ -49,10 +49,8 @@ def test_fp8_forward_only_and_llama2_workload():
     torch.cuda.synchronize()
     assert torch.equal(fwd.loss, full.loss) and torch.equal(fwd.lse, full.lse)
     ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f32(Hb),
-                      Wg=flce_inputs.bf16_bits_to_f32(Wb))
-    errs = compare(full, ref)
-    print(errs)
-    assert_within(errs)
+                      Wg=flce_inputs.bf16_bits_to_f32(Wb), want_abs=True)
+    oracle_check(full, Hb, Wb, y, ref)
 
 
 @pytest.mark.parametrize("opts", [{"v_chunk": 512, "n_block": 256},
@@ -65,24 +63,8 @@ def test_fp8_token_blocks_and_chunks(opts):
     res = flce.forward_backward_fp8(H8, sh, W8, sw, lab, H, W, **opts)
     assert flce.check_status(res.status) == flce.FLCE_OK
     ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
-                      Wg=flce_inputs.bf16_bits_to_f64(Wb))
-    errs = compare(res, ref)
-    print(errs)
-    assert_within(errs)
-
-
-def _quantize_expected(bits):
-    """Per-tensor E4M3 quantisation as flce_quantize_e4m3 states it: scale = amax / 448
-    and inv = 448 / amax rounded to fp32 (inv capped at the largest finite fp32; both 1
-    for an all-zero tensor), the product x * inv in fp32, then the nearest E4M3 code
-    (flce_inputs.e4m3_encode)."""
-    x = flce_inputs.bf16_bits_to_f32(bits).astype(np.float32)
-    amax = np.float32(np.max(np.abs(x)))
-    scale = np.float32(float(amax) / 448.0) if amax > 0 else np.float32(1.0)
-    big = float(np.finfo(np.float32).max)
-    inv = np.float32(min(448.0 / float(amax), big)) if amax > 0 else np.float32(1.0)
-    y = (x * inv).astype(np.float32)
-    return flce_inputs.e4m3_encode(y.astype(np.float64)), scale, amax
+                      Wg=flce_inputs.bf16_bits_to_f64(Wb), want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref, opts)
 
 
 def _wide_range_bf16(shape, seed):
@@ -95,6 +77,8 @@ def _wide_range_bf16(shape, seed):
 
 @pytest.mark.parametrize("case", ["normal", "wide", "zeros", "tiny", "ragged_grid", "subnormal"])
 def test_device_quantizer_matches_its_definition(case):
+    """flce_quantize_e4m3 bit for bit against the oracle's per-tensor E4M3
+    quantisation (oracle/e4m3.py, pinned by its properties on the CPU)."""
     if case == "normal":
         bits = flce_inputs.normal_bf16((300, 256), 0.05, seed=3, stream=0)
     elif case == "wide":
@@ -109,7 +93,8 @@ def test_device_quantizer_matches_its_definition(case):
         bits = flce_inputs.f32_to_bf16_bits(x)
     else:  # more 8-element groups than one grid pass covers
         bits = _wide_range_bf16((4099, 2056), seed=6)
-    q_ref, scale_ref, amax_ref = _quantize_expected(bits)
+    r = e4m3.quantize_per_tensor(flce_inputs.bf16_bits_to_f32(bits))
+    q_ref, scale_ref, amax_ref = r["codes"], r["scale"], r["amax"]
     x = torch.from_numpy(bits.view(np.int16)).to("cuda:0").view(torch.bfloat16)
     q, out = flce.quantize_e4m3(x)
     torch.cuda.synchronize()
@@ -131,10 +116,8 @@ def test_device_quantized_operands_feed_the_fp8_path():
     res = flce.forward_backward_fp8(H8, oh[0:1], W8, ow[0:1], lab, H, W)
     assert flce.check_status(res.status) == flce.FLCE_OK
     torch.cuda.synchronize()
-    He = flce_inputs.e4m3_decode(H8.cpu().numpy()) * np.float64(oh[0].item())
-    We = flce_inputs.e4m3_decode(W8.cpu().numpy()) * np.float64(ow[0].item())
+    He = e4m3.e4m3_decode(H8.cpu().numpy()) * np.float64(oh[0].item())
+    We = e4m3.e4m3_decode(W8.cpu().numpy()) * np.float64(ow[0].item())
     ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
-                      Wg=flce_inputs.bf16_bits_to_f64(Wb))
-    errs = compare(res, ref)
-    print(errs)
-    assert_within(errs)
+                      Wg=flce_inputs.bf16_bits_to_f64(Wb), want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref)

@@ -400,3 +400,68 @@ def test_gradient_operands_enter_only_the_two_products():
     # dW is linear in Hg: dW(Hg) - dW(H) = dW computed with (Hg - H)
     c = oracle.flce(H, W, y, Hg=Hg - H, Wg=W)
     np.testing.assert_allclose(b["dW"] - a["dW"], c["dW"], rtol=1e-10, atol=1e-14)
+
+
+# ---- magnitude products (the rounding scale of each gradient element) ------------
+
+def test_magnitude_products_zero_weights_closed_form():
+    """W = 0: g_iv = (1/V - [y_i = v]) / n, so |G|^T |H| has the closed form
+    sum_valid (|1/V - [y_i = v]| / n) |h_i| and |G| |W| = 0."""
+    N, D, V = 7, 5, 11
+    g = np.random.default_rng(41)
+    H = g.standard_normal((N, D))
+    y = np.array([3, -100, 0, 10, 3, -100, 7])
+    r = oracle.flce(H, np.zeros((V, D)), y, want_abs=True)
+    n = 5
+    expect = np.zeros((V, D))
+    for i in range(N):
+        if y[i] == -100:
+            continue
+        for v in range(V):
+            expect[v] += abs(1.0 / V - (1.0 if v == y[i] else 0.0)) / n * np.abs(H[i])
+    np.testing.assert_allclose(r["dW_abs"], expect, rtol=0, atol=1e-15)
+    assert np.all(r["dH_abs"] == 0.0)
+
+
+def test_magnitude_products_brute_force():
+    """Loops over the definition g_iv = (exp(z_iv - lse_i) - [v = y_i]) * scale with
+    lse from mpmath, then sum_v |g_iv| |w_vd| and sum_i |g_iv| |h_id|; selected rows,
+    ignored tokens and a gradient scale included."""
+    N, D, V = 6, 4, 9
+    H, W, y = _rand(42, N, D, V, scale=0.7)
+    y[2] = -100
+    rows, vids = np.array([0, 2, 5]), np.array([1, 4, 8])
+    r = oracle.flce(H, W, y, grad_scale=0.3, dh_rows=rows, dw_rows=vids, want_abs=True)
+    n = 5
+    G = np.zeros((N, V))
+    for i in range(N):
+        if y[i] == -100:
+            continue
+        z = [sum(float(H[i, d]) * float(W[v, d]) for d in range(D)) for v in range(V)]
+        lse = float(mpmath.log(mpmath.fsum(mpmath.exp(mpmath.mpf(t)) for t in z)))
+        for v in range(V):
+            G[i, v] = (math.exp(z[v] - lse) - (1.0 if v == y[i] else 0.0)) * 0.3 / n
+    for k, i in enumerate(rows):
+        for d in range(D):
+            want = sum(abs(G[i, v]) * abs(W[v, d]) for v in range(V))
+            assert r["dH_abs"][k, d] == pytest.approx(want, rel=1e-12, abs=1e-15)
+    for k, v in enumerate(vids):
+        for d in range(D):
+            want = sum(abs(G[i, v]) * abs(H[i, d]) for i in range(N))
+            assert r["dW_abs"][k, d] == pytest.approx(want, rel=1e-12, abs=1e-15)
+
+
+def test_magnitude_products_bound_and_equal_the_signed_ones_without_cancellation():
+    """|dH| <= |G||W| and |dW| <= |G|^T|H| everywhere (triangle inequality), with
+    equality for the dW row of an id that no token has as its label when H >= 0
+    (every g_iv of that column is then positive, so nothing cancels)."""
+    N, D, V = 40, 16, 30
+    H, W, y = _rand(43, N, D, V, scale=0.5)
+    H = np.abs(H)
+    y = np.where(y == 7, 8, y)   # id 7: no hits
+    y[::9] = -100
+    r = oracle.flce(H, W, y, want_abs=True)
+    assert np.all(np.abs(r["dH"]) <= r["dH_abs"] * (1 + 1e-12))
+    assert np.all(np.abs(r["dW"]) <= r["dW_abs"] * (1 + 1e-12))
+    np.testing.assert_allclose(r["dW"][7], r["dW_abs"][7], rtol=1e-13, atol=0)
+    assert np.all(r["dH_abs"][y == -100] == 0.0)

@@ -12,7 +12,7 @@ import pytest
 
 import flce_inputs
 import oracle
-from flce_testlib import assert_within, compare, to_device
+from flce_testlib import oracle_check, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -60,10 +60,26 @@ def test_vocabulary_shards_combine_to_the_oracle(bounds):
     Hb, Wb, y = flce_inputs.make_inputs(wl)
     H, W, lab = to_device(Hb, Wb, y)
     res = _run_shards(H, W, lab, bounds, V)
-    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y)
-    errs = compare(res, ref)
-    print(errs)
-    assert_within(errs)
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y,
+                      want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref, dh_f32=True)
+
+
+def test_whole_vocabulary_shard_softmax_part_in_fp32():
+    """One shard holding the whole vocabulary returns dH in fp32, before any
+    rounding to bf16, so the softmax part of dH is gated at 5e-3 with no output
+    rounding in the budget: only G's one rounding per entry and fp32 sums. The
+    Llama-2-like weight scale, several chunks and token blocks."""
+    N, D, V = 1000, 512, 8000
+    wl = flce_inputs.Workload("shard_whole", N, D, V, 1.0, 0.02, "uniform", 0.05, seed=34)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H, W, lab = to_device(Hb, Wb, y)
+    plan = {"v_chunk": 2048, "n_block": 512}
+    res = _run_shards(H, W, lab, [0, V], V, fwd_opts=plan, bwd_opts=plan)
+    ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y,
+                      want_abs=True)
+    errs = oracle_check(res, Hb, Wb, y, ref, dh_f32=True)
+    assert errs["dH_soft_rel"] <= 5e-3
 
 
 def test_shard_plans_sum_reduction_and_bf16_dw():
@@ -78,10 +94,9 @@ def test_shard_plans_sum_reduction_and_bf16_dw():
     res = _run_shards(H, W, lab, [0, 1300, 2600], V, fwd_opts=plan,
                       bwd_opts=dict(plan, grad_scale=0.5, dw_dtype="bfloat16"), reduction="sum")
     ref = oracle.flce(flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb), y,
-                      reduction="sum", grad_scale=0.5)
-    errs = compare(res, ref)
-    print(errs)
-    assert_within(errs)
+                      reduction="sum", grad_scale=0.5, want_abs=True)
+    oracle_check(res, Hb, Wb, y, ref, {"reduction": "sum", "grad_scale": 0.5,
+                                       "dw_dtype": "bfloat16"}, dh_f32=True)
 
 
 def test_shard_label_outside_the_whole_vocabulary_sets_status():
