@@ -10,9 +10,12 @@ Reported (one JSON line on rank 0):
   tflops     8*N*V*D flops per step / step time (forward, recompute, two gradient GEMMs)
   e2e        tokens/s through the public API with host buffers: H, W and labels
              copied from pinned host memory and the loss read back, every step
-  roofline   the tcgen05 GEMM kernel (every heavy launch of the step) against the
-             measured bf16 matmul peak
-  cpu_baseline  the float64 CPU oracle timed on a bounded sample of the workload
+  roofline   the dominant tcgen05 GEMM kernel (dW and dH launches) and each of the
+             four products against the measured bf16 matmul peak (burst; the
+             sustained peak beside it)
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample of the workload, a
+                labelled extrapolation to the full step, and the tiny workload on
+                one core
   peak_extra_hbm_bytes  the library's workspace (its whole extra device memory)
                         next to the N*V*4 bytes of fp32 logits an unfused head holds
 
@@ -62,22 +65,22 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_RECORDS = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
 def measured_traffic(kernel: str, workload: str, v_chunk: int):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary (profiles/dram_traffic_*.md lines 'traffic kernel=... workload=...
-    v_chunk=... bytes_per_launch=... kernel_sha=...'); None when absent, when the
-    plan differs, or when the kernel sources changed since the counters were taken."""
-    import glob
+    """DRAM bytes per launch of `kernel` on `workload` from the committed record of
+    ncu captures (profiles/dram_traffic.json); None when absent, when the plan
+    differs, or when the kernel sources changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_RECORDS):
+        return None
     sha = kernel_source_sha()
-    for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
-        with open(path) as f:
-            for line in f:
-                if not line.startswith("traffic "):
-                    continue
-                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
-                if kv.get("kernel") == kernel and kv.get("workload") == workload \
-                        and kv.get("kernel_sha") == sha and kv.get("v_chunk") == str(v_chunk):
-                    return float(kv["bytes_per_launch"])
+    with open(TRAFFIC_RECORDS) as f:
+        records = json.load(f).get("records", [])
+    for r in records:
+        if r.get("kernel") == kernel and r.get("workload") == workload \
+                and r.get("kernel_sha") == sha and int(r.get("v_chunk", -1)) == int(v_chunk):
+            return float(r["bytes_per_launch"])
     return None
 
 
@@ -202,6 +205,62 @@ def cpu_oracle_sample(wl, tokens: int) -> dict:
     return {"seconds": dt, "tokens": tokens}
 
 
+def oracle_tiny_single_core() -> dict:
+    """The float64 oracle on the whole tiny workload (64 x 128 x 1000), fwd+bwd, in a
+    child process whose BLAS is limited to one thread (best of 5 after a warm-up)."""
+    code = ("import time, flce_inputs, oracle\n"
+            "wl = flce_inputs.get('tiny')\n"
+            "Hb, Wb, y = flce_inputs.make_inputs(wl)\n"
+            "H, W = flce_inputs.bf16_bits_to_f64(Hb), flce_inputs.bf16_bits_to_f64(Wb)\n"
+            "oracle.flce(H, W, y)\n"
+            "best = 1e9\n"
+            "for _ in range(5):\n"
+            "    t0 = time.perf_counter(); oracle.flce(H, W, y); best = min(best, time.perf_counter() - t0)\n"
+            "print(best)\n")
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    env["PYTHONPATH"] = ROOT + os.pathsep + env.get("PYTHONPATH", "")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=120, cwd=ROOT)
+        sec = float(r.stdout.strip().splitlines()[-1])
+    except Exception as e:   # reported, never fatal
+        return {"error": str(e)[:200]}
+    N = flce_inputs.get("tiny").N
+    return {"seconds": sec, "tokens_per_s": N / sec, "cores": 1,
+            "sample": "the whole tiny workload (N=64, D=128, V=1000), float64 fwd+bwd, best of 5"}
+
+
+def fp8_reference_tflops(H8, W8, sh, sw, stream, reps: int = 10) -> dict:
+    """cuBLASLt's E4M3 GEMM (torch._scaled_mm, bf16 output) on the same operands,
+    Z = H8 W8^T at the LSE product's shape: the measured FP8 denominator."""
+    import torch
+    M, K = H8.shape
+    Nn = W8.shape[0]
+    try:
+        a = H8.view(torch.float8_e4m3fn)
+        b = W8.view(torch.float8_e4m3fn).t()   # [K, N] column-major
+        s_a, s_b = sh[0:1].reshape(()), sw[0:1].reshape(())
+        out = torch.empty(M, Nn, dtype=torch.bfloat16, device=H8.device)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                torch._scaled_mm(a, b, scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16, out=out)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            best = 1e9
+            for _ in range(reps):
+                e0.record()
+                torch._scaled_mm(a, b, scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16, out=out)
+                e1.record()
+                e1.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+        del out
+        return {"tflops": 2.0 * M * Nn * K / (best * 1e-3) / 1e12, "ms_best": best,
+                "how": f"torch._scaled_mm E4M3 x E4M3 -> bf16, {M} x {Nn} x {K}, best of {reps}"}
+    except Exception as e:
+        return {"tflops": None, "error": str(e)[:300]}
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -252,7 +311,7 @@ def run_forward_only(args, wl, world, rank, local):
     W = torch.from_numpy(Wb.view(np.int16)).to(dev).view(torch.bfloat16)
     lab = torch.from_numpy(y).to(dev)
     N, D, V = wl.N, wl.D, wl.V
-    ws = torch.empty(flce.workspace_size(N, D, V), dtype=torch.uint8, device=dev)
+    ws = torch.empty(flce.forward_workspace_size(N, D, V), dtype=torch.uint8, device=dev)
     out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
            "lse": torch.empty(N, dtype=torch.float32, device=dev)}
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -278,12 +337,14 @@ def run_forward_only(args, wl, world, rank, local):
         rep.barrier()
     ms = rep.max(ev0.elapsed_time(ev1) / args.steps)
     tflops = 2.0 * N * V * D / (ms / 1e3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
     line = {"metric": "FLCE forward (loss + lse) tokens/s", "value": N * world / (ms / 1e3),
             "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded; no dataset or weights)",
-            "config": config_block(wl, world), "tflops": tflops, "frac_bf16_peak": tflops / peak,
+            "config": config_block(wl, world), "tflops": tflops, "frac_bf16_peak": tflops / burst,
+            "frac_bf16_peak_sustained": tflops / sustained,
             "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -621,28 +682,38 @@ def main(argv=None) -> int:
     flops = 8.0 * N * V * D
     tflops = flops / (ms / 1e3) / 1e12
     value = N * world / (ms / 1e3)
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
     gemm_flops = 2.0 * N * V * D   # per step, for each of the four products
 
     def rate(ms_per_step):
         return gemm_flops / (ms_per_step / 1e3) / 1e12 if ms_per_step > 0 else None
 
     # The dominant kernel: the tcgen05 GEMM with the fp32 epilogue (dW = G^T H and
-    # dH = G W launches), half of the step's flops and the largest time share.
+    # dH = G W launches), half of the step's flops and the largest time share. The
+    # kernels are timed as launches inside a step well under a second long, so the
+    # burst cuBLAS peak is the denominator; the sustained one is reported beside it.
     f32_ms = kernel_ms["dw_gemm"] + kernel_ms["dh_gemm"]
     f32_launches = n_kind["dw_gemm"] + n_kind["dh_gemm"]
     achieved = 2.0 * gemm_flops / (f32_ms / 1e3) / 1e12
+    products = {}
+    for name, k in (("lse", "lse_gemm"), ("gradient", "grad_gemm"), ("dW", "dw_gemm"),
+                    ("dH", "dh_gemm")):
+        r = rate(kernel_ms[k])
+        products[name] = {"kernel": k, "tflops": r, "frac": r / burst,
+                          "frac_of_sustained": r / sustained}
     roofline = {
         "bound": "tensor", "unit": "TFLOP/s",
         "kernel": "flce_gemm_kernel<EPI_F32> (tcgen05: dW = G^T H and dH = G W launches)",
-        "achieved": achieved, "peak": peak, "frac": achieved / peak,
-        "peak_kind": f"bf16 cuBLAS sustained, {peaks['source']} (burst {peaks['bf16_tflops']})",
-        "frac_of_burst": achieved / peaks["bf16_tflops"],
+        "achieved": achieved, "peak": burst, "frac": achieved / burst,
+        "peak_kind": f"bf16 cuBLAS burst, {peaks['source']} (MEASURED_PEAKS.json bf16_tflops)",
+        "peak_sustained": sustained, "frac_of_sustained": achieved / sustained,
+        "products": products,
         "launches_per_step": f32_launches // args.steps,
         "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / args.steps),
         "ms_per_launch_avg": (per_kind["dw_gemm"] + per_kind["dh_gemm"]) / max(f32_launches, 1),
         "traffic": measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name, plan["v_chunk"]),
-        "traffic_source": "profiles/dram_traffic_*.md (ncu dram__bytes_read.sum + "
+        "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
                           "dram__bytes_write.sum per launch; null if the kernel changed)",
         "kernel_sha": kernel_source_sha(),
         "kernels": {k: {"ms_per_step": kernel_ms[k], "ms_per_launch": kernel_launch_ms[k],
@@ -657,22 +728,36 @@ def main(argv=None) -> int:
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # N = 1 only
         r = cpu_oracle_sample(wl, min(args.cpu_tokens, wl.N))
+        full_s = r["seconds"] * wl.N / r["tokens"]
         cpu = {"value": r["tokens"] / r["seconds"], "unit": UNIT, "cores": blas_threads(),
                "kind": "oracle", "seconds": r["seconds"],
                "sample": f"first {r['tokens']} tokens of the {wl.name} workload, full V={V} "
-                         f"and D={D}, float64 fwd+bwd (loss, lse, dH, dW)"}
+                         f"and D={D}, float64 fwd+bwd (loss, lse, dH, dW)",
+               "extrapolated_full": {
+                   "seconds_per_step": full_s, "tokens_per_s": wl.N / full_s,
+                   "method": f"EXTRAPOLATED, not measured: sample seconds x N / sample tokens "
+                             f"({wl.N} / {r['tokens']}); the oracle's work is linear in N at "
+                             f"fixed V and D (logits, lse, dH and dW passes: about 8 N V D "
+                             f"float64 flops)"},
+               "tiny_single_core": oracle_tiny_single_core()}
 
     if fp8 is not None:
-        # the two logits products run on E4M3 operands: their peak is the measured
-        # bf16 peak x the nominal FP8/bf16 ratio (4.5 / 2.25 PFLOP/s dense)
-        fp8_peak = 2.0 * peak
-        for k in ("lse_gemm", "grad_gemm"):
+        # the two logits products run on E4M3 operands: their denominator is cuBLASLt's
+        # own E4M3 GEMM (torch._scaled_mm) timed in this process at the LSE product's
+        # shape; the nominal FP8/bf16 ratio (4.5 / 2.25 PFLOP/s dense) x the measured
+        # bf16 peak only if that GEMM cannot run here
+        fp8_ref = fp8_reference_tflops(fp8[0], fp8[2], fp8[1], fp8[3], stream)
+        fp8_peak = fp8_ref["tflops"] if fp8_ref.get("tflops") else 2.0 * burst
+        for name, k in (("lse", "lse_gemm"), ("gradient", "grad_gemm")):
             roofline["kernels"][k]["peak_fp8"] = fp8_peak
             roofline["kernels"][k]["frac_of_fp8_peak"] = roofline["kernels"][k]["tflops"] / fp8_peak
-        roofline["note_fp8"] = ("lse_gemm and grad_gemm use E4M3 operands (kind::f8f6f4); "
-                                "peak_fp8 = 2 x the measured bf16 peak (nominal ratio); each "
-                                "step first quantises H and W on the device (amax + E4M3 "
-                                "kernels, 2 launches per tensor)")
+            products[name]["frac"] = products[name]["tflops"] / fp8_peak
+            products[name]["peak"] = fp8_peak
+        roofline["fp8_reference"] = fp8_ref
+        roofline["note_fp8"] = ("lse_gemm and grad_gemm use E4M3 operands (kind::f8f6f4); their "
+                                "fractions are against fp8_reference (cuBLASLt E4M3 GEMM at the "
+                                "LSE shape, same process); each step first quantises H and W "
+                                "on the device (amax + E4M3 kernels, 2 launches per tensor)")
         q_bytes = (N + V) * D * (2 + 2 + 1)   # amax read, quantise read + write
         roofline["quantize"] = {"ms_per_step": quant_ms, "algorithmic_bytes": q_bytes,
                                 "gbs": q_bytes / (quant_ms * 1e-3) / 1e9}
@@ -681,7 +766,8 @@ def main(argv=None) -> int:
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 logits products + bf16 gradient products" if fp8 else "bf16", "data": "synthetic (seeded; no dataset or weights)",
         "config": config_block(wl, world),
-        "tflops": tflops, "frac_bf16_peak": tflops / peak,
+        "tflops": tflops, "frac_bf16_peak": tflops / burst,
+        "frac_bf16_peak_sustained": tflops / sustained,
         "ms_per_step_stats": step_stats,
         "peak_extra_hbm_bytes": int(peak_delta),
         "workspace_bytes": ws_bytes, "allocator_peak_delta_bytes": int(peak_delta),

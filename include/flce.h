@@ -118,9 +118,22 @@ void flce_default_options(flce_options* opt);
  * vocabulary spans several chunks, an fp32 [n_block, D] dH accumulator (plus an
  * fp32 [V, D] dW accumulator only for bf16 dW with several token blocks). It is
  * the whole extra device memory of a call and is far below the N*V*4 bytes of
- * fp32 logits. Returns FLCE_OK and writes *bytes, or an error code.
+ * fp32 logits. Returns FLCE_OK and writes *bytes, or an error code
+ * (FLCE_ERR_NULL, FLCE_ERR_SHAPE, FLCE_ERR_ALIGN for D % 8 != 0, FLCE_ERR_OPTION).
  */
 int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt, size_t* bytes);
+
+/*
+ * Bytes of device workspace that the forward-only calls (flce_forward,
+ * flce_forward_fp8, flce_forward_shard) need: the forward pieces of
+ * flce_workspace_size without the G chunk and the dH / dW accumulators,
+ *     align256(8 * S * 256 * ceil(N / 256)) + 3 * align256(4 * N) + 256 bytes,
+ * S = opt->v_splits (vocabulary ranges per 128-token block; 0 = the largest
+ * count the planner can choose, min(ceil(V / 256), 128), so that the size does
+ * not depend on the device). Independent of D. Same errors as flce_workspace_size.
+ */
+int flce_forward_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt,
+                                size_t* bytes);
 
 /*
  * Describe the plan for an (N, D, V) problem on the current device: token
@@ -134,7 +147,15 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
                   int32_t want_dw, flce_plan_info* info);
 
 /*
- * Loss, per-token LSE and both gradients in one call.
+ * Loss, per-token LSE and both gradients in one call: the fused linear
+ * cross-entropy forward and backward of "Liger Kernel: Fused Triton Kernels for
+ * LLM Training", section "The Architecture" (1. the logits tile by tile with an
+ * online log-sum-exp and the target logit taken on the fly, only the loss and
+ * the per-token log-sum-exp kept; 2. the logits recomputed from that
+ * log-sum-exp, dL/dz = softmax - one-hot formed in the kernel, dL/dH = (dL/dz) W
+ * and dL/dW = (dL/dz)^T H), with the 1/N mean of the page's Python simulation
+ * and the argument layout of the GPU MODE lecture 28 notes, cross-entropy
+ * section (hidden states (B*S, hidden), LM-head weight (vocab, hidden), labels).
  *   H       bf16 [N, D]   hidden states (input)
  *   W       bf16 [V, D]   LM-head weight (input)
  *   labels  int32 [N]     target ids in [0, V) or ignore_index (input)
@@ -154,10 +175,14 @@ int flce_forward_backward(const uint16_t* H, const uint16_t* W, const int32_t* l
 
 /*
  * Forward only: the loss and (optionally) lse, without any gradient work (the
- * evaluation path). Same arguments and rules as flce_forward_backward, except
- * that with reduction FLCE_REDUCTION_NONE `loss` is fp32 [N]: each token's
- * lse_i - z_{i,y_i}, and 0 for ignored tokens (the per-token loss of PyTorch's
- * reduction="none").
+ * evaluation path): "Liger Kernel: Fused Triton Kernels for LLM Training",
+ * section "The Architecture", 1. (chunked logits, online log-sum-exp, target
+ * logit extraction; nothing of size N x V stored). Same arguments and rules as
+ * flce_forward_backward, except that the workspace need only hold
+ * flce_forward_workspace_size() bytes and that with reduction
+ * FLCE_REDUCTION_NONE `loss` is fp32 [N]: each token's lse_i - z_{i,y_i}, and 0
+ * for ignored tokens (the per-token loss of PyTorch's reduction="none", which the
+ * GPU MODE lecture 28 notes' drop-in replaces).
  */
 int flce_forward(const uint16_t* H, const uint16_t* W, const int32_t* labels, int64_t N, int64_t D,
                  int64_t V, const flce_options* opt, float* loss, float* lse, void* workspace,
@@ -262,15 +287,25 @@ int flce_quantize_e4m3(const uint16_t* x, int64_t n, uint8_t* q, float* out, voi
  *   - Arguments and results are those of flce_forward without the workspace;
  *     the caller still passes H, W, labels, loss, lse and status.
  *   - Scratch is one 32 MiB array in device memory owned by the library. Every
- *     GPU that loads it keeps it until the process exits. The call allocates
- *     nothing (no cudaMalloc, no cudaFree, no allocating library routine).
- *   - Limit: problems whose forward scratch exceeds 32 MiB are rejected with
- *     FLCE_ERR_WORKSPACE before anything is enqueued. The scratch is about
- *     20 bytes per token plus 512 * D bytes, so at D = 4096 up to about
- *     1.5 million tokens fit.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     GPU that loads it keeps it until the process exits. The entry point calls
+ *     no cudaMalloc, cudaFree or allocating library routine.
+ *   - Set-up, once per device: the array is created when the CUDA runtime loads
+ *     this part of the library on a device, which with CUDA's default lazy
+ *     module loading is the first call on that device (the first call then also
+ *     looks up the array's device address with that device current). That first
+ *     call can therefore take 32 MiB of device memory and fail with
+ *     FLCE_ERR_CUDA if none is left; every later call on the device allocates
+ *     nothing. Callers that reserve memory up front should make the set-up call
+ *         flce_forward_noalloc(NULL, NULL, NULL, 0, 0, 0, NULL, NULL, NULL, NULL, NULL)
+ *     (it does only the set-up on the current device and returns FLCE_OK or
+ *     FLCE_ERR_CUDA) on each device before reserving their pool, and before any
+ *     stream capture.
+ *   - Limit: the forward scratch, flce_forward_workspace_size() with the
+ *     planned S (1 or 2 for large N), about 20 bytes per token and independent
+ *     of D and V, must fit in 32 MiB: about 1.6 million tokens. A planned S is
+ *     lowered until the partials fit; a caller's explicit opt->v_splits is kept.
+ *     Problems that do not fit are rejected with FLCE_ERR_WORKSPACE before
+ *     anything is enqueued.
  *   - Every call shares the one array, and it keeps the last call's contents.
  *     Nothing in it needs clearing between calls, because each call writes every
  *     scratch word before reading it. Calls whose work overlaps on the GPU (on

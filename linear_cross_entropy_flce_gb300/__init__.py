@@ -9,8 +9,9 @@ from ._binding import (FLCE_ERR_ALIGN, FLCE_ERR_CUDA, FLCE_ERR_DEVICE, FLCE_ERR_
                        FLCE_ERR_NULL, FLCE_ERR_OPTION, FLCE_ERR_SHAPE, FLCE_ERR_TIMEOUT,
                        FLCE_ERR_WORKSPACE, FLCE_OK, FLCEError, LIB_PATH, Options, Result,
                        ShardForward, backward_shard, ce_logits, check_status, forward,
-                       forward_backward, forward_backward_fp8, forward_shard, get_plan, lib,
-                       make_options, quantize_e4m3, scale_grads, status_string, workspace_size)
+                       forward_backward, forward_backward_fp8, forward_noalloc, forward_shard,
+                       forward_workspace_size, get_plan, lib, make_options, noalloc_setup,
+                       quantize_e4m3, scale_grads, status_string, workspace_size)
 from .loss import (FusedLinearCrossEntropyFunction, FusedLinearCrossEntropyLoss,
                    fused_linear_cross_entropy)
 
@@ -18,7 +19,8 @@ __all__ = ["FLCE_ERR_ALIGN", "FLCE_ERR_CUDA", "FLCE_ERR_DEVICE", "FLCE_ERR_LABEL
            "FLCE_ERR_NULL", "FLCE_ERR_OPTION", "FLCE_ERR_SHAPE", "FLCE_ERR_TIMEOUT",
            "FLCE_ERR_WORKSPACE", "FLCE_OK", "FLCEError", "LIB_PATH", "Options", "Result",
            "ShardForward", "backward_shard", "ce_logits", "check_status", "forward",
-           "forward_backward", "forward_backward_fp8", "forward_shard", "get_plan", "lib",
-           "make_options", "quantize_e4m3", "scale_grads", "status_string", "workspace_size",
+           "forward_backward", "forward_backward_fp8", "forward_noalloc", "forward_shard",
+           "forward_workspace_size", "get_plan", "lib", "make_options", "noalloc_setup",
+           "quantize_e4m3", "scale_grads", "status_string", "workspace_size",
            "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
            "fused_linear_cross_entropy"]

@@ -74,6 +74,12 @@ lib.flce_default_options.restype = None
 lib.flce_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options),
                                     ctypes.POINTER(ctypes.c_size_t)]
 lib.flce_workspace_size.restype = ctypes.c_int
+lib.flce_forward_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options),
+                                            ctypes.POINTER(ctypes.c_size_t)]
+lib.flce_forward_workspace_size.restype = ctypes.c_int
+lib.flce_forward_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.POINTER(Options),
+                                     _vp, _vp, _vp, _vp]
+lib.flce_forward_noalloc.restype = ctypes.c_int
 lib.flce_get_plan.argtypes = [_i64, _i64, _i64, ctypes.POINTER(Options), ctypes.c_int32,
                               ctypes.c_int32, ctypes.POINTER(PlanInfo)]
 lib.flce_get_plan.restype = ctypes.c_int
@@ -157,6 +163,16 @@ def workspace_size(N: int, D: int, V: int, opts: Optional[Options] = None) -> in
                                  ctypes.byref(out))
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_workspace_size")
+    return int(out.value)
+
+
+def forward_workspace_size(N: int, D: int, V: int, opts: Optional[Options] = None) -> int:
+    """Workspace bytes of the forward-only calls (flce_forward_workspace_size)."""
+    out = ctypes.c_size_t(0)
+    rc = lib.flce_forward_workspace_size(N, D, V, ctypes.byref(opts) if opts is not None else None,
+                                         ctypes.byref(out))
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_workspace_size")
     return int(out.value)
 
 
@@ -263,9 +279,8 @@ def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=
     lse = out.get("lse")
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
-    ws_bytes = workspace_size(N, D, V, opts)
     if workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        workspace = torch.empty(forward_workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     if stream is None:
@@ -276,6 +291,41 @@ def forward(H, W, labels, *, out: Optional[dict] = None, workspace=None, status=
     if rc != FLCE_OK:
         raise FLCEError(rc, "flce_forward")
     return Result(loss, lse, None, None, status)
+
+
+def forward_noalloc(H, W, labels, *, out: Optional[dict] = None, status=None, stream=None,
+                    **options) -> Result:
+    """Loss and lse via flce_forward_noalloc: the library's own static scratch
+    instead of a workspace (for callers that cannot allocate at call time)."""
+    import torch
+    N, D, V = _check_inputs(H, W, labels)
+    opts = make_options(**options)
+    dev = H.device
+    out = dict(out or {})
+    loss = out.get("loss")
+    if loss is None:
+        loss = torch.empty(N if options.get("reduction") == "none" else 1, dtype=torch.float32,
+                           device=dev)
+    lse = out.get("lse")
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.flce_forward_noalloc(_ptr(H), _ptr(W), _ptr(labels), N, D, V, ctypes.byref(opts),
+                                  _ptr(loss), _ptr(lse), _ptr(status), stream)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_noalloc")
+    return Result(loss, lse, None, None, status)
+
+
+def noalloc_setup() -> None:
+    """The set-up call of flce_forward_noalloc on the current device (creates the
+    library's static scratch there and looks up its address)."""
+    rc = lib.flce_forward_noalloc(None, None, None, 0, 0, 0, None, None, None, None, None)
+    if rc != FLCE_OK:
+        raise FLCEError(rc, "flce_forward_noalloc set-up")
 
 
 @dataclasses.dataclass
@@ -299,7 +349,7 @@ def forward_shard(H, W_shard, labels, v_offset: int, V_total: int, *, out: Optio
     m, s_, zt = (out.get(k) if out.get(k) is not None else
                  torch.empty(N, dtype=torch.float32, device=dev) for k in ("m", "s", "zt"))
     if workspace is None:
-        workspace = torch.empty(workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(forward_workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     if stream is None:
@@ -474,7 +524,8 @@ def forward_backward_fp8(H8, scale_h, W8, scale_w, labels, H=None, W=None, *,
         dt = torch.float32 if options.get("dw_dtype", "float32") == "float32" else torch.bfloat16
         dW = torch.empty(V, D, dtype=dt, device=dev)
     if workspace is None:
-        workspace = torch.empty(workspace_size(N, D, V, opts), dtype=torch.uint8, device=dev)
+        size = workspace_size if grads else forward_workspace_size
+        workspace = torch.empty(size(N, D, V, opts), dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     if stream is None:

@@ -197,7 +197,10 @@ int choose_splits(int m_blocks, int v_tiles, int sms) {
   return best;
 }
 
-int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, Plan* P) {
+// backward = false: only the forward pieces (partials, target logits, NLL, lse,
+// scalars); the G chunk and the dH / dW accumulators are left out of the total.
+int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, Plan* P,
+              bool backward = true) {
   Plan p;
   p.N = N;
   p.D = D;
@@ -250,9 +253,13 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
   p.off_nll = take(static_cast<size_t>(N) * 4);
   p.off_lse = take(static_cast<size_t>(N) * 4);
   p.off_scal = take(256);
-  p.off_g = take(static_cast<size_t>(rows_b) * cv * 2);
-  p.off_dhacc = p.need_dh_acc ? take(static_cast<size_t>(rows_b) * D * 4) : off;
-  p.off_dwacc = p.need_dw_acc ? take(static_cast<size_t>(V) * D * 4) : off;
+  if (backward) {
+    p.off_g = take(static_cast<size_t>(rows_b) * cv * 2);
+    p.off_dhacc = p.need_dh_acc ? take(static_cast<size_t>(rows_b) * D * 4) : off;
+    p.off_dwacc = p.need_dw_acc ? take(static_cast<size_t>(V) * D * 4) : off;
+  } else {
+    p.off_g = p.off_dhacc = p.off_dwacc = off;
+  }
   p.total = off;
   *P = p;
   return FLCE_OK;
@@ -372,7 +379,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   rc = device_info(&sms);
   if (rc != FLCE_OK) return rc;
   Plan P;
-  rc = make_plan(N, D, V, o, sms, &P);
+  rc = make_plan(N, D, V, o, sms, &P, backward);
   if (rc != FLCE_OK) return rc;
   if (ws_bytes < P.total) return FLCE_ERR_WORKSPACE;
   if (backward && o.reduction == FLCE_REDUCTION_NONE) {
@@ -621,6 +628,29 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   return FLCE_OK;
 }
 
+int workspace_bytes(int64_t N, int64_t D, int64_t V, const flce_options* opt, bool backward,
+                    size_t* bytes) {
+  if (bytes == nullptr) return FLCE_ERR_NULL;
+  flce_options o;
+  flce_default_options(&o);
+  if (opt != nullptr) o = *opt;
+  int rc = flce::check_shape(N, D, V);
+  if (rc != FLCE_OK) return rc;
+  rc = flce::check_options(o);
+  if (rc != FLCE_OK) return rc;
+  // The vocabulary-range split count depends on the SM count; plan for the
+  // largest split count that choose_splits can return so that the size does not
+  // depend on the device (and can be asked for without one).
+  flce_options big = o;
+  if (big.v_splits == 0) big.v_splits = static_cast<int32_t>(std::min<int64_t>(
+                                            flce::ceil_div(V, flce::BN), 128));
+  flce::Plan P;
+  rc = flce::make_plan(N, D, V, big, 1, &P, backward);
+  if (rc != FLCE_OK) return rc;
+  *bytes = P.total;
+  return FLCE_OK;
+}
+
 }  // namespace
 }  // namespace flce
 
@@ -638,25 +668,12 @@ void flce_default_options(flce_options* opt) {
 }
 
 int flce_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt, size_t* bytes) {
-  if (bytes == nullptr) return FLCE_ERR_NULL;
-  flce_options o;
-  flce_default_options(&o);
-  if (opt != nullptr) o = *opt;
-  int rc = flce::check_shape(N, D, V);
-  if (rc != FLCE_OK) return rc;
-  rc = flce::check_options(o);
-  if (rc != FLCE_OK) return rc;
-  // The vocabulary-range split count depends on the SM count; plan for the
-  // largest split count that choose_splits can return so that the size does not
-  // depend on the device (and can be asked for without one).
-  flce_options big = o;
-  if (big.v_splits == 0) big.v_splits = static_cast<int32_t>(std::min<int64_t>(
-                                            flce::ceil_div(V, flce::BN), 128));
-  flce::Plan P;
-  rc = flce::make_plan(N, D, V, big, 1, &P);
-  if (rc != FLCE_OK) return rc;
-  *bytes = P.total;
-  return FLCE_OK;
+  return flce::workspace_bytes(N, D, V, opt, true, bytes);
+}
+
+int flce_forward_workspace_size(int64_t N, int64_t D, int64_t V, const flce_options* opt,
+                                size_t* bytes) {
+  return flce::workspace_bytes(N, D, V, opt, false, bytes);
 }
 
 int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int32_t want_dh,
@@ -676,7 +693,7 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
   rc = flce::device_info(&sms);
   if (rc != FLCE_OK) return rc;
   flce::Plan P;
-  rc = flce::make_plan(N, D, V, o, sms, &P);
+  rc = flce::make_plan(N, D, V, o, sms, &P, want_dh != 0 || want_dw != 0);
   if (rc != FLCE_OK) return rc;
   info->n_block = P.n_block;
   info->v_chunk = P.v_chunk;

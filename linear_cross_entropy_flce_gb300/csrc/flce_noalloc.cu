@@ -11,7 +11,11 @@
 // How: the scratch that flce_forward would take from the caller's workspace
 // lives here in one file-scope __device__ array of kNoAllocScratchBytes. Every
 // GPU that loads this part of the library keeps that array until the process
-// exits. Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+// exits. Nothing here calls cudaMalloc, cudaFree or any allocating routine, but
+// the array itself comes into being when the CUDA runtime loads this file's
+// device code on a device; with lazy module loading (the default) that happens
+// at the first cudaGetSymbolAddress below, i.e. during the first call on that
+// device, which is therefore the set-up call.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -54,32 +58,33 @@ int scratch_address(void** out) {
 extern "C" int flce_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* labels,
                                     int64_t N, int64_t D, int64_t V, const flce_options* opt,
                                     float* loss, float* lse, int32_t* status, void* stream) {
+  void* scratch = nullptr;
+  // The set-up form: no problem, only the array's creation and address lookup on
+  // the current device.
+  if (H == nullptr && W == nullptr && labels == nullptr && loss == nullptr && lse == nullptr &&
+      status == nullptr && N == 0 && D == 0 && V == 0)
+    return scratch_address(&scratch);
   flce_options o;
   flce_default_options(&o);
   if (opt != nullptr) o = *opt;
-  // The forward pass never touches the backward's G chunk or accumulators, but the
-  // size check it shares with flce_forward_backward counts them: pin them to their
-  // smallest plan so that nearly all of the array serves the forward pass.
-  o.v_chunk = 256;
-  o.n_block = 128;
-  o.dw_dtype = FLCE_DTYPE_F32;
-  if (o.v_splits == 0) {
+  const bool planned = o.v_splits == 0;
+  if (planned) {
     flce_plan_info info;
     const int rc = flce_get_plan(N, D, V, &o, 0, 0, &info);
     if (rc != FLCE_OK) return rc;
     o.v_splits = info.v_splits;
   }
   size_t need = 0;
-  int rc = flce_workspace_size(N, D, V, &o, &need);
+  int rc = flce_forward_workspace_size(N, D, V, &o, &need);
   if (rc != FLCE_OK) return rc;
-  // Fewer vocabulary ranges need fewer partials; halve until the plan fits.
-  while (need > kNoAllocScratchBytes && o.v_splits > 1) {
+  // A planned split count may be lowered until the partials fit (fewer
+  // vocabulary ranges need fewer partials); a caller's explicit one is kept.
+  while (planned && need > kNoAllocScratchBytes && o.v_splits > 1) {
     o.v_splits = (o.v_splits + 1) / 2;
-    rc = flce_workspace_size(N, D, V, &o, &need);
+    rc = flce_forward_workspace_size(N, D, V, &o, &need);
     if (rc != FLCE_OK) return rc;
   }
   if (need > kNoAllocScratchBytes) return FLCE_ERR_WORKSPACE;
-  void* scratch = nullptr;
   rc = scratch_address(&scratch);
   if (rc != FLCE_OK) return rc;
   // Every scratch word the forward pass reads is written earlier in the same

@@ -31,6 +31,14 @@ int main(void) {
   CHECK(flce_workspace_size(0, 4096, 128256, &o, &bytes) == FLCE_ERR_SHAPE);
   CHECK(flce_workspace_size(8, 64, 100, &o, NULL) == FLCE_ERR_NULL);
   CHECK(flce_ce_workspace_size(8192, 128256, NULL, &bytes) == FLCE_OK && bytes > 0);
+  {
+    /* the forward-only size leaves out the G chunk and accumulators, and not D */
+    size_t fwd = 0, fwd2 = 0, full = 0;
+    CHECK(flce_forward_workspace_size(8192, 4096, 128256, &o, &fwd) == FLCE_OK);
+    CHECK(flce_forward_workspace_size(8192, 64, 128256, &o, &fwd2) == FLCE_OK && fwd2 == fwd);
+    CHECK(flce_workspace_size(8192, 4096, 128256, &o, &full) == FLCE_OK && fwd < full);
+    CHECK(flce_forward_workspace_size(8192, 4100, 128256, &o, &fwd) == FLCE_ERR_ALIGN);
+  }
   CHECK(flce_forward_backward(NULL, NULL, NULL, 8, 64, 100, &o, NULL, NULL, NULL, NULL, NULL, 0,
                               NULL, NULL) == FLCE_ERR_NULL);
   {

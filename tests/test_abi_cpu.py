@@ -21,7 +21,8 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    assert names == sorted(["flce_default_options", "flce_workspace_size", "flce_get_plan",
+    assert names == sorted(["flce_default_options", "flce_workspace_size",
+                            "flce_forward_workspace_size", "flce_get_plan",
                             "flce_forward_backward", "flce_forward", "flce_forward_noalloc",
                             "flce_ce_workspace_size", "flce_ce_logits", "flce_forward_fp8",
                             "flce_forward_backward_fp8", "flce_quantize_e4m3",
@@ -54,6 +55,31 @@ def test_workspace_is_far_below_logits():
         ws = flce.workspace_size(N, D, V)
         assert 0 < ws < N * V * 4 * frac, (N, D, V, ws)
         assert ws < 600 << 20
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("N,D,V,S", [(1_000_000, 4096, 128256, 1), (8192, 4096, 128256, 2),
+                                     (300, 200, 1500, 3)])
+def test_forward_workspace_matches_the_header_formula(N, D, V, S):
+    """flce_forward_workspace_size against the formula include/flce.h states:
+    align256(8 S 256 ceil(N/256)) + 3 align256(4 N) + 256, independent of D."""
+    want = _align256(8 * S * 256 * (-(-N // 256))) + 3 * _align256(4 * N) + 256
+    opts = flce.make_options(v_splits=S)
+    assert flce.forward_workspace_size(N, D, V, opts) == want
+    assert flce.forward_workspace_size(N, 8 * D, V, opts) == want
+    assert flce.forward_workspace_size(N, D, V, opts) < flce.workspace_size(N, D, V, opts)
+
+
+def test_noalloc_limit_stated_in_the_header():
+    """The no-workspace entry point's scratch is 32 MiB: with S = 1, about 20 bytes
+    per token fit about 1.6 million tokens, whatever D and V."""
+    one = flce.make_options(v_splits=1)
+    assert flce.forward_workspace_size(1_600_000, 4096, 128256, one) <= 32 << 20
+    assert flce.forward_workspace_size(1_700_000, 4096, 128256, one) > 32 << 20
+    assert flce.forward_workspace_size(2_000_000, 8, 256, one) > 32 << 20
 
 
 def test_workspace_grows_with_requested_chunk():
