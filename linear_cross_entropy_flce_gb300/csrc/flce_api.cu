@@ -147,6 +147,12 @@ bool encode_g_chunked(CUtensorMap* m, void* G, uint64_t rows, uint64_t v_chunk, 
 
 // Tiles are computed by cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int kCtaGroup = 2;
+// The dW product (K = the token block, 8192 at the Llama-3-8B head) runs 256 x 512
+// tiles: a quarter fewer operand bytes per flop and fewer distinct operand rows per
+// wave, for an epilogue that no longer overlaps the next tile (about 1% of a tile
+// that long). The dH product keeps 256 x 256 tiles.
+constexpr bool kWideDw = true;
+constexpr bool kWideDh = false;
 
 // MN-major bf16 operand [rows][mn] (mn contiguous, mn % 64 == 0, row stride ld
 // elements) as a 3-D map [mn/64][rows][64] read in boxes of 64 x box_rows x
@@ -550,7 +556,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         w.b_box3 = d_box3 ? 1 : 0;
         w.b_k0 = static_cast<int>(b0);
         w.m_blocks = static_cast<int>(ceil_div(c_len, P.tile_m));
-        w.n_blocks = static_cast<int>(ceil_div(D, BN));
+        w.n_blocks = static_cast<int>(ceil_div(D, kWideDw ? 2 * BN : BN));
         w.k_blocks = static_cast<int>(ceil_div(nb_len, BK));
         w.num_units = w.m_blocks * w.n_blocks;
         w.group_m = std::min(w.m_blocks, 8);
@@ -572,7 +578,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         if (!encode_out(&mDW, dw_base, dw_direct_bf16, D, c_len, D)) return FLCE_ERR_CUDA;
         w.out_row0 = 0;
         w.out_mode = dw_direct_bf16 ? OUT_STORE_BF16 : (b == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
-        if (launch_gemm_f32(cta, mG_mn, mH_mn, mDW, w, cta * std::min(w.num_units, pairs), st) !=
+        if (launch_gemm_f32(cta, mG_mn, mH_mn, mDW, w, cta * std::min(w.num_units, pairs), st,
+                            kWideDw ? 1 : 0) !=
                 cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;
@@ -587,7 +594,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         h.b_box3 = d_box3 ? 1 : 0;
         h.b_k0 = static_cast<int>(c0);
         h.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
-        h.n_blocks = static_cast<int>(ceil_div(D, BN));
+        h.n_blocks = static_cast<int>(ceil_div(D, kWideDh ? 2 * BN : BN));
         h.k_blocks = static_cast<int>(ceil_div(c_len, BK));
         h.num_units = h.m_blocks * h.n_blocks;
         h.group_m = std::min(h.m_blocks, 8);
@@ -609,7 +616,8 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         if (!ok_dh) return FLCE_ERR_CUDA;
         h.out_row0 = 0;
         h.out_mode = dh_direct ? OUT_STORE_BF16 : (c == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
-        if (launch_gemm_f32(cta, mG_k, mW_mn, mDH, h, cta * std::min(h.num_units, pairs), st) !=
+        if (launch_gemm_f32(cta, mG_k, mW_mn, mDH, h, cta * std::min(h.num_units, pairs), st,
+                            kWideDh ? 1 : 0) !=
                 cudaSuccess ||
             !trace())
           return FLCE_ERR_CUDA;

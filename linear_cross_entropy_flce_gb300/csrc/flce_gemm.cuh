@@ -170,12 +170,17 @@ __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, 
 // stage row, multiplied with tcgen05 kind::f8f6f4; the epilogue scales z by
 // the product of the two device scales. The shared-memory image of a stage is
 // the same as for bf16.
-template <int kEpi, int kCta, int kFp8 = 0>
+// kWide = 1: 256 x 512 tiles (TileCfg): each CTA stages two 128-row halves of B
+// per K block, the MMA thread issues one N = 256 MMA per half into columns
+// [256 h, 256 h + 256) of the single accumulator, and tile column c is product
+// column n_blk * 512 + c.
+template <int kEpi, int kCta, int kFp8 = 0, int kWide = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using Cfg = TileCfg<kCta>;
+  using Cfg = TileCfg<kCta, kWide>;
+  static_assert(kWide == 0 || kEpi == EPI_F32, "wide tiles carry the fp32 epilogue only");
   constexpr int kStages = Cfg::kStages;
   constexpr int kSub = Cfg::kSub;
   const int k_stages = (p.k_blocks + kSub - 1) / kSub;  // ring stages per tile
@@ -264,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // copies complete on the even CTA's barrier
             const uint32_t fb = (kCta == 2) ? mapa_shared(fb_local, 0) : fb_local;
             const int am = m_blk * Cfg::kTileM + static_cast<int>(rank) * BM;   // A rows
-            const int bn = n_blk * BN + static_cast<int>(rank) * Cfg::kBRows;   // B rows
             auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t pol) {
               if constexpr (kCta == 2) tma_load_2d_pair(dst, map, x, y, fb, pol);
               else tma_load_2d_hint(dst, map, x, y, fb, pol);
@@ -290,14 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < BM / 64; ++j)
                   load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
               }
-              if (!p.b_mn_major) {
-                load(sb, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
-              } else if (p.b_box3) {
-                load3(sb, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
-              } else {
 #pragma unroll
-                for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                  load(sb + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+              for (int h = 0; h < Cfg::kBHalves; ++h) {
+                // B rows of this CTA for the MMA of tile columns [256 h, 256 h + 256)
+                const int bn = n_blk * Cfg::kTileN + h * BN + static_cast<int>(rank) * Cfg::kBRows;
+                const uint32_t sbh = sb + h * Cfg::kBHalfBytes;
+                if (!p.b_mn_major) {
+                  load(sbh, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
+                } else if (p.b_box3) {
+                  load3(sbh, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                    load(sbh + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+                }
               }
             }
             }
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kTileN);
           for (int kq = 0; kq < k_stages; ++kq) {
             const bool full_ok = mbar_wait_bounded<kCl>(full_bar(stage), phase, tmo, abort_flag);
             if (!__all_sync(0xffffffffu, full_ok)) {
@@ -387,11 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < BK / UK; ++k) {
                 const uint64_t da = a_mn ? make_sw128_desc(sa + k * (UK * 128), kMnBoxBytes, 1024)
                                          : make_sw128_desc(sa + k * (UK * 2), 16, 1024);
-                const uint64_t db = b_mn ? make_sw128_desc(sb + k * (UK * 128), kMnBoxBytes, 1024)
-                                         : make_sw128_desc(sb + k * (UK * 2), 16, 1024);
                 const uint32_t accum = (kq | sub | k) != 0 ? 1u : 0u;   // first MMA of the tile overwrites
-                if constexpr (kFp8) umma_f8_cg<kCta>(d_tmem, da, db, p.idesc, accum);
-                else umma_bf16_cg<kCta>(d_tmem, da, db, p.idesc, accum);
+#pragma unroll
+                for (int h = 0; h < Cfg::kBHalves; ++h) {
+                  const uint32_t sbh = sb + h * Cfg::kBHalfBytes;
+                  const uint64_t db = b_mn ? make_sw128_desc(sbh + k * (UK * 128), kMnBoxBytes, 1024)
+                                           : make_sw128_desc(sbh + k * (UK * 2), 16, 1024);
+                  const uint32_t dh = d_tmem + static_cast<uint32_t>(h * BN);
+                  if constexpr (kFp8) umma_f8_cg<kCta>(dh, da, db, p.idesc, accum);
+                  else umma_bf16_cg<kCta>(dh, da, db, p.idesc, accum);
+                }
               }
             }
             umma_commit_pair<kCta>(empty_bar(stage));  // frees the stage in both CTAs
@@ -406,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (elect_one()) umma_commit_pair<kCta>(tfull_bar(acc));
           __syncwarp();
-          if (++acc == 2) {
+          if (++acc == Cfg::kAccs) {
             acc = 0;
             acc_phase ^= 1u;
           }
@@ -485,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * Cfg::kTileN);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < Cfg::kTileN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_wait_ld();
@@ -498,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] *= acc_scale;
           }
-          const int col = n_blk * BN + c * 32;  // product column
+          const int col = n_blk * Cfg::kTileN + c * 32;  // product column
           if constexpr (kEpi == EPI_LSE) {
             lse_chunk(v, col, p.n_valid, y - (p.col_base + col), st);
           } else {
@@ -535,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kCta == 2) mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
           else mbar_arrive(tempty_bar(acc));
         }
-        if (++acc == 2) {
+        if (++acc == Cfg::kAccs) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -566,6 +581,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_cg<kCta>(tmem_base, kTmemCols);
+}
+
+// Host-side launch of one instantiation: grid/kCta clusters of kCta CTAs, the tile
+// configuration's dynamic shared memory, the three tensor maps and the parameters
+// passed by value (the LSE epilogue ignores the output map c).
+template <int kEpi, int kCta, int kFp8, int kWide>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const GemmParams& p, int grid, cudaStream_t stream) {
+  auto kern = flce_gemm_kernel<kEpi, kCta, kFp8, kWide>;
+  constexpr size_t smem = TileCfg<kCta, kWide>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
 }
 
 }  // namespace flce

@@ -26,14 +26,25 @@ constexpr uint32_t kMnBoxBytes = 64 * BK * 2;  // one 64(MN) x 64(K) MN-major bo
 // tensor pipe queues little work ahead, so with cta_group::2 two K blocks (eight
 // MMAs) share each wait and commit; three 64 KB stages keep as many bytes in flight
 // as six 32 KB ones.
-template <int kCta>
+// kWide = 1 (pair only): a 256 x 512 tile, two N = 256 MMAs per K step sharing the A
+// block, one accumulator of all 512 TMEM columns. Each SM stages 48 KB per K block
+// for twice the MMAs of a 32 KB block (a quarter fewer operand bytes per flop, and
+// each wave of tiles touches fewer distinct operand rows), four stages of one K
+// block (eight MMAs each); the epilogue no longer overlaps the next tile's MMAs,
+// which only long-K products (dW, dH) can afford.
+template <int kCta, int kWide = 0>
 struct TileCfg {
-  static constexpr int kSub = kCta == 2 ? 2 : 1;   // K blocks per ring stage
-  static constexpr int kStages = kCta == 2 ? 3 : 4;
+  static_assert(kWide == 0 || kCta == 2, "the wide tile is a cluster-pair tile");
+  static constexpr int kSub = kWide ? 1 : (kCta == 2 ? 2 : 1);   // K blocks per ring stage
+  static constexpr int kStages = kWide ? 4 : (kCta == 2 ? 3 : 4);
   static constexpr int kTileM = BM * kCta;         // rows of the tile (both CTAs)
-  static constexpr int kBRows = BN / kCta;         // rows of B (tile columns) per CTA
+  static constexpr int kTileN = kWide ? 2 * BN : BN;  // columns of the tile
+  static constexpr int kBHalves = kWide ? 2 : 1;   // N = 256 MMAs per K step
+  static constexpr int kAccs = kWide ? 1 : 2;      // TMEM accumulators of kTileN columns
+  static constexpr int kBRows = BN / kCta;         // rows of B (tile columns) per CTA and MMA
   static constexpr uint32_t kABytes = BM * BK * 2;
-  static constexpr uint32_t kBBytes = kBRows * BK * 2;
+  static constexpr uint32_t kBHalfBytes = kBRows * BK * 2;
+  static constexpr uint32_t kBBytes = kBHalves * kBHalfBytes;
   static constexpr uint32_t kSubBytes = kABytes + kBBytes;    // one K block, per CTA
   static constexpr uint32_t kStageBytes = kSub * kSubBytes;   // one ring stage, per CTA
   // Epilogue staging for TMA stores: two 4 KB boxes (32 rows x 128 bytes) per
@@ -41,6 +52,7 @@ struct TileCfg {
   static constexpr uint32_t kStgBytes = 4096;
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   static constexpr size_t kSmemBytes = 1024 + kRingBytes + 4 * 2 * kStgBytes + 256;
+  static_assert(kSmemBytes <= 232448, "more dynamic shared memory than a CTA may have");
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

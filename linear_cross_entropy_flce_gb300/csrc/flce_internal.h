@@ -17,6 +17,8 @@ namespace flce {
 // the device scales p.acc_scale_h, p.acc_scale_w.
 // c is the output map of the epilogue's TMA stores (unused by the LSE epilogue):
 // bf16 G for the gradient GEMM; fp32 (or bf16 for OUT_STORE_BF16) for the F32 one.
+// wide = 1 (F32 only): 256 x 512 tiles (TileCfg<2, 1>); p.n_blocks then counts
+// 512-column tiles.
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
@@ -24,7 +26,7 @@ cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensor
                              cudaStream_t stream, int fp8);
 cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const CUtensorMap& c, const GemmParams& p, int grid,
-                            cudaStream_t stream);
+                            cudaStream_t stream, int wide);
 
 // Per-token merge of the vocabulary-range partials into lse and the per-token
 // negative log-likelihood.
