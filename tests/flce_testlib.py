@@ -265,6 +265,19 @@ def assert_within(errs: dict):
             assert v <= 1.0, (k, errs)
 
 
+def dw_sample_groups(y, vids, V, n_frequent=32):
+    """Positions in vids of the three kinds of sampled vocabulary ids, gated apart:
+    id V-1, the most frequent label ids, and the uniform picks (mostly ids that no
+    token has as its label, whose dW row is all softmax part)."""
+    ids, counts = np.unique(y[y != -100], return_counts=True)
+    top = set(int(v) for v in ids[np.argsort(-counts, kind="stable")[:n_frequent]])
+    groups = {"last": [], "frequent": [], "uniform": []}
+    for k, v in enumerate(vids):
+        key = "last" if v == V - 1 else "frequent" if int(v) in top else "uniform"
+        groups[key].append(k)
+    return {k: np.asarray(g, dtype=np.int64) for k, g in groups.items() if g}
+
+
 def oracle_check(res, Hb, Wb, y, ref, opts=None, **kw) -> dict:
     """compare() with the bf16 inputs as the gradient operands, then assert_within."""
     errs = compare(res, ref, labels=y, Hg=flce_inputs.bf16_bits_to_f64(Hb),

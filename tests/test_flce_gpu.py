@@ -6,7 +6,8 @@ import pytest
 
 import flce_inputs
 import oracle
-from flce_testlib import assert_within, bf16_tensor_to_f64, compare, oracle_check, tensor_to_f64, to_device
+from flce_testlib import (assert_within, bf16_tensor_to_f64, compare, dw_sample_groups, oracle_check,
+                          tensor_to_f64, to_device)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -201,19 +202,6 @@ def test_llama2_like_workload_full_parity():
     _run_and_compare(Hb, Wb, y)
 
 
-def dw_sample_groups(y, vids, V, n_frequent=32):
-    """Positions in vids of the three kinds of sampled vocabulary ids, gated apart:
-    id V-1, the most frequent label ids, and the uniform picks (mostly ids that no
-    token has as its label, whose dW row is all softmax part)."""
-    ids, counts = np.unique(y[y != -100], return_counts=True)
-    top = set(int(v) for v in ids[np.argsort(-counts, kind="stable")[:n_frequent]])
-    groups = {"last": [], "frequent": [], "uniform": []}
-    for k, v in enumerate(vids):
-        key = "last" if v == V - 1 else "frequent" if int(v) in top else "uniform"
-        groups[key].append(k)
-    return {k: np.asarray(g, dtype=np.int64) for k, g in groups.items() if g}
-
-
 @pytest.mark.parametrize("name", ["llama3_8b", "qwen2_7b", "long_seq"])
 def test_full_size_workload_sampled_parity(name):
     """Full-size workloads in the default plan (the launch configuration the
@@ -241,6 +229,20 @@ def test_full_size_workload_sampled_parity(name):
     assert_within(errs)
     # no [N, V] buffer: the whole extra device memory is the declared workspace
     assert flce.workspace_size(wl.N, wl.D, wl.V) < wl.N * wl.V * 4 // 8
+    if name == "long_seq":
+        # bf16 dW over the plan's four token blocks: the fp32 dW accumulator in the
+        # workspace, added to in launch order, rounded once at the end
+        del res
+        H, W, lab = to_device(Hb, Wb, y)
+        r16 = flce.forward_backward(H, W, lab, dw_dtype="bfloat16")
+        assert flce.check_status(r16.status) == flce.FLCE_OK
+        assert flce.get_plan(wl.N, wl.D, wl.V)["n_blocks"] > 1
+        del H, W
+        errs16 = compare(r16, ref, dh_rows=torch.from_numpy(rows).to(dev),
+                         dw_rows=torch.from_numpy(vids).to(dev), labels=y, Hg=Hf, Wg=Wf,
+                         opts={"dw_dtype": "bfloat16"}, dw_groups=groups)
+        print(name, "bf16 dW", errs16)
+        assert_within(errs16)
 
 
 def test_bounded_wait_timeout_sets_status_and_context_stays_usable():

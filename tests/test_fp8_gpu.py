@@ -7,7 +7,7 @@ import pytest
 import flce_inputs
 import oracle
 from oracle import e4m3
-from flce_testlib import oracle_check, to_device
+from flce_testlib import assert_within, compare, dw_sample_groups, oracle_check, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -121,3 +121,31 @@ def test_device_quantized_operands_feed_the_fp8_path():
     ref = oracle.flce(He, We, y, Hg=flce_inputs.bf16_bits_to_f64(Hb),
                       Wg=flce_inputs.bf16_bits_to_f64(Wb), want_abs=True)
     oracle_check(res, Hb, Wb, y, ref)
+
+
+def test_fp8_full_size_llama3_workload_sampled_parity():
+    """The FP8 variant at the Llama-3-8B-shaped head in the launch configuration the
+    benchmark times (operands quantised on the device, scales read from device
+    memory): loss and every lse against the oracle over the dequantised operands,
+    dH on 256 sampled tokens and dW on 64 sampled ids in their three groups, the
+    softmax part and the element-wise bound included."""
+    wl = flce_inputs.get("llama3_8b")
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H, W, lab = to_device(Hb, Wb, y)
+    H8, oh = flce.quantize_e4m3(H)
+    W8, ow = flce.quantize_e4m3(W)
+    res = flce.forward_backward_fp8(H8, oh[0:1], W8, ow[0:1], lab, H, W)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    He = (e4m3.e4m3_decode(H8.cpu().numpy()) * np.float64(oh[0].item())).astype(np.float32)
+    We = (e4m3.e4m3_decode(W8.cpu().numpy()) * np.float64(ow[0].item())).astype(np.float32)
+    del H, W, H8, W8
+    rows = oracle.sample_rows(y, 256, seed=wl.seed)
+    vids = oracle.sample_vocab(y, wl.V, 64, seed=wl.seed)
+    Hf, Wf = flce_inputs.bf16_bits_to_f32(Hb), flce_inputs.bf16_bits_to_f32(Wb)
+    ref = oracle.flce(He, We, y, Hg=Hf, Wg=Wf, dh_rows=rows, dw_rows=vids, want_abs=True)
+    dev = res.lse.device
+    errs = compare(res, ref, dh_rows=torch.from_numpy(rows).to(dev),
+                   dw_rows=torch.from_numpy(vids).to(dev), labels=y, Hg=Hf, Wg=Wf,
+                   dw_groups=dw_sample_groups(y, vids, wl.V))
+    print(errs)
+    assert_within(errs)
