@@ -56,6 +56,20 @@ def test_small_and_degenerate_shapes(N, D, V):
     _run_and_compare(Hb, Wb, y)
 
 
+@pytest.mark.parametrize("N,D,V,opts", [
+    (300, 576, 1500, {}),                          # second 256-wide half of tile 1 wholly past D
+    (257, 704, 2049, {"v_chunk": 1024}),           # half 0 of tile 1 ragged, half 1 past D
+    (520, 1088, 3000, {"n_block": 256, "dw_dtype": "bfloat16"}),  # 2 tiles + 64 columns, bf16 dW over token blocks
+    (130, 840, 700, {}),                           # D % 64 != 0: two-box MN-major loads, halves past D
+])
+def test_wide_dw_tile_edges(N, D, V, opts):
+    """The dW product's 256 x 512 tiles where D is not a multiple of 512: a tile's
+    second N = 256 half lies partly or wholly past D (its B rows read the zero fill
+    of the copy engine, its output columns are clipped by the store map)."""
+    Hb, Wb, y = _inputs(N, D, V, seed=N + D + V, p_ignore=0.05)
+    _run_and_compare(Hb, Wb, y, **opts)
+
+
 def test_labels_at_vocabulary_edges():
     Hb, Wb, y = _inputs(256, 128, 1000, seed=5)
     y[:64] = 0
