@@ -147,12 +147,15 @@ bool encode_g_chunked(CUtensorMap* m, void* G, uint64_t rows, uint64_t v_chunk, 
 
 // Tiles are computed by cluster pairs (tcgen05 cta_group::2, 256-row tiles).
 constexpr int kCtaGroup = 2;
-// The dW product (K = the token block, 8192 at the Llama-3-8B head) runs 256 x 512
-// tiles: a quarter fewer operand bytes per flop and fewer distinct operand rows per
-// wave, for an epilogue that no longer overlaps the next tile (about 1% of a tile
-// that long). The dH product keeps 256 x 256 tiles.
+// The dW and dH products (K = the token block / the vocabulary chunk, 8192 and
+// 16032 at the Llama-3-8B head) run 256 x 512 tiles: a quarter fewer operand bytes
+// per flop and fewer distinct operand rows per wave, for an epilogue that no longer
+// overlaps the next tile (about 1% of a tile that long). Requested together they
+// share one launch, dH's tiles first, because dH alone has too few wide tiles to
+// fill the pairs (256 for 76 pairs at the Llama-3-8B head: a last wave 37% full);
+// dH alone keeps 256 x 256 tiles.
 constexpr bool kWideDw = true;
-constexpr bool kWideDh = false;
+constexpr bool kWideDhAlone = false;
 
 // MN-major bf16 operand [rows][mn] (mn contiguous, mn % 64 == 0, row stride ld
 // elements) as a 3-D map [mn/64][rows][64] read in boxes of 64 x box_rows x
@@ -547,9 +550,11 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
           !trace())
         return FLCE_ERR_CUDA;
 
+      const bool both = dW != nullptr && want_dh;
+      GemmArgs aw{}, ah{};
       if (dW != nullptr) {
         // dW rows [c0, c0 + c_len) (+)= G_bc^T H_b: M = vocabulary, N = hidden, K = tokens.
-        GemmParams w{};
+        GemmParams& w = aw.p;
         w.a_mn_major = 1;
         w.b_mn_major = 1;
         w.a_box3 = 1;
@@ -570,31 +575,28 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         w.m_valid = c_len;
         w.n_valid = static_cast<int>(D);
         // the map holds exactly the chunk's rows, so ragged tiles are clipped
-        CUtensorMap mDW;
         const int64_t dw_off = c0 * D;
         void* dw_base = dw_direct_bf16 ? static_cast<void*>(static_cast<uint16_t*>(dW) + dw_off)
                         : dw_bf16      ? static_cast<void*>(dw_acc + dw_off)
                                        : static_cast<void*>(static_cast<float*>(dW) + dw_off);
-        if (!encode_out(&mDW, dw_base, dw_direct_bf16, D, c_len, D)) return FLCE_ERR_CUDA;
+        if (!encode_out(&aw.c, dw_base, dw_direct_bf16, D, c_len, D)) return FLCE_ERR_CUDA;
+        aw.a = mG_mn;
+        aw.b = mH_mn;
         w.out_row0 = 0;
         w.out_mode = dw_direct_bf16 ? OUT_STORE_BF16 : (b == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
-        if (launch_gemm_f32(cta, mG_mn, mH_mn, mDW, w, cta * std::min(w.num_units, pairs), st,
-                            kWideDw ? 1 : 0) !=
-                cudaSuccess ||
-            !trace())
-          return FLCE_ERR_CUDA;
       }
 
+      const bool wide_dh = both || kWideDhAlone;
       if (want_dh) {
         // dH rows [b0, b0 + nb_len) (+)= G_bc W_c: M = tokens, N = hidden, K = vocabulary.
-        GemmParams h{};
+        GemmParams& h = ah.p;
         h.a_mn_major = 0;
         h.a_kchunk = 1;
         h.b_mn_major = 1;
         h.b_box3 = d_box3 ? 1 : 0;
         h.b_k0 = static_cast<int>(c0);
         h.m_blocks = static_cast<int>(ceil_div(nb_len, P.tile_m));
-        h.n_blocks = static_cast<int>(ceil_div(D, kWideDh ? 2 * BN : BN));
+        h.n_blocks = static_cast<int>(ceil_div(D, wide_dh ? 2 * BN : BN));
         h.k_blocks = static_cast<int>(ceil_div(c_len, BK));
         h.num_units = h.m_blocks * h.n_blocks;
         h.group_m = std::min(h.m_blocks, 8);
@@ -608,20 +610,29 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
         // block's rows (stored by chunk 0, reduce-added by the others), rounded
         // to bf16 after the last chunk. The map holds exactly the block's rows.
         // A shard accumulates straight into its fp32 dH part.
-        CUtensorMap mDH;
         const bool dh_direct = P.n_chunks == 1 && !shard;
-        const bool ok_dh = shard ? encode_out(&mDH, sh.dh_f32 + b0 * D, false, D, nb_len, D)
-                           : dh_direct ? encode_out(&mDH, dH + b0 * D, true, D, nb_len, D)
-                                       : encode_out(&mDH, dh_acc, false, D, nb_len, D);
+        const bool ok_dh = shard ? encode_out(&ah.c, sh.dh_f32 + b0 * D, false, D, nb_len, D)
+                           : dh_direct ? encode_out(&ah.c, dH + b0 * D, true, D, nb_len, D)
+                                       : encode_out(&ah.c, dh_acc, false, D, nb_len, D);
         if (!ok_dh) return FLCE_ERR_CUDA;
+        ah.a = mG_k;
+        ah.b = mW_mn;
         h.out_row0 = 0;
         h.out_mode = dh_direct ? OUT_STORE_BF16 : (c == 0 ? OUT_STORE_F32 : OUT_ADD_F32);
-        if (launch_gemm_f32(cta, mG_k, mW_mn, mDH, h, cta * std::min(h.num_units, pairs), st,
-                            kWideDh ? 1 : 0) !=
-                cudaSuccess ||
-            !trace())
-          return FLCE_ERR_CUDA;
       }
+      // dW and dH both read only G (and H, W), and write different outputs
+      cudaError_t ge = cudaSuccess;
+      if (both) {
+        const int units = ah.p.num_units + aw.p.num_units;
+        ge = launch_gemm_f32_pair(cta, ah, aw, cta * std::min(units, pairs), st);
+      } else if (dW != nullptr) {
+        ge = launch_gemm_f32(cta, aw.a, aw.b, aw.c, aw.p, cta * std::min(aw.p.num_units, pairs),
+                             st, kWideDw ? 1 : 0);
+      } else if (want_dh) {
+        ge = launch_gemm_f32(cta, ah.a, ah.b, ah.c, ah.p, cta * std::min(ah.p.num_units, pairs),
+                             st, wide_dh ? 1 : 0);
+      }
+      if (ge != cudaSuccess || ((dW != nullptr || want_dh) && !trace())) return FLCE_ERR_CUDA;
     }
     if (dH != nullptr && !shard && P.n_chunks > 1 &&
         (launch_f32_to_bf16(dh_acc, dH + b0 * D, static_cast<int64_t>(nb_len) * D, sms, st) !=
@@ -709,9 +720,10 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
   info->n_chunks = P.n_chunks;
   info->v_splits = P.splits;
   // LSE GEMM, merge, reduce; per token block: per chunk the gradient GEMM and
-  // the dW / dH GEMMs asked for, then (several chunks) the bf16 rounding of dH;
-  // bf16 dW over several token blocks: one rounding of its accumulator at the end.
-  const int per_chunk = 1 + (want_dh ? 1 : 0) + (want_dw ? 1 : 0);
+  // one launch of the dW and / or dH products asked for, then (several chunks) the
+  // bf16 rounding of dH; bf16 dW over several token blocks: one rounding of its
+  // accumulator at the end.
+  const int per_chunk = 1 + ((want_dh || want_dw) ? 1 : 0);
   const int per_block = P.n_chunks * per_chunk + ((want_dh && P.n_chunks > 1) ? 1 : 0);
   const bool dw_round = want_dw && o.dw_dtype == FLCE_DTYPE_BF16 && P.n_nblocks > 1;
   info->kernel_launches =

@@ -174,16 +174,23 @@ __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, 
 // per K block, the MMA thread issues one N = 256 MMA per half into columns
 // [256 h, 256 h + 256) of the single accumulator, and tile column c is product
 // column n_blk * 512 + c.
-template <int kEpi, int kCta, int kFp8 = 0, int kWide = 0>
+// kProducts = 2: one launch computes two independent products of the same tile
+// shape and epilogue, g0's units first, then g1's (the dH and dW products of a
+// vocabulary chunk, which both only read G). Units are dealt to the pairs in that
+// fixed order, each unit taking its maps and parameters from its own product, so
+// every output element still has one writer per launch.
+template <int kEpi, int kCta, int kFp8 = 0, int kWide = 0, int kProducts = 1>
 __global__ void __launch_bounds__(kThreads, 1)
-    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    flce_gemm_kernel(const __grid_constant__ GemmArgs g0, const __grid_constant__ GemmArgs g1) {
   using Cfg = TileCfg<kCta, kWide>;
   static_assert(kWide == 0 || kEpi == EPI_F32, "wide tiles carry the fp32 epilogue only");
+  static_assert(kProducts == 1 || kEpi == EPI_F32, "two products per launch: fp32 epilogue only");
   constexpr int kStages = Cfg::kStages;
   constexpr int kSub = Cfg::kSub;
-  const int k_stages = (p.k_blocks + kSub - 1) / kSub;  // ring stages per tile
+  // settings shared by every unit of the launch come from the first product
+  const GemmParams& p0 = g0.p;
+  const int units0 = p0.num_units;
+  const int total_units = units0 + (kProducts == 2 ? g1.p.num_units : 0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -222,9 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if constexpr (kEpi != EPI_LSE) tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&g0.a);
+    tma_prefetch_desc(&g0.b);
+    if constexpr (kEpi != EPI_LSE) tma_prefetch_desc(&g0.c);
+    if constexpr (kProducts == 2) {
+      tma_prefetch_desc(&g1.a);
+      tma_prefetch_desc(&g1.b);
+      tma_prefetch_desc(&g1.c);
+    }
   }
   // Barriers of both CTAs are initialised before either CTA touches the other's.
   if constexpr (kCta == 2) cluster_sync();
@@ -237,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
-  const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo = p0.timeout_ns;
 
   if (warp == 0) {
     // ---------------- TMA producer (each CTA loads its own A rows and B half) -----
@@ -246,12 +258,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
-      const uint64_t pol_a = make_l2_policy(p.a_hint);
-      const uint64_t pol_b = make_l2_policy(p.b_hint);
+      const uint64_t pol_a = make_l2_policy(p0.a_hint);
+      const uint64_t pol_b = make_l2_policy(p0.b_hint);
       int tile_it = 0;
-      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
+      for (int u = pair; ok && u < total_units; u += num_pairs) {
+        const bool second = kProducts == 2 && u >= units0;
+        const GemmArgs& G = second ? g1 : g0;
+        const GemmParams& p = G.p;
+        const int k_stages = (p.k_blocks + kSub - 1) / kSub;  // ring stages per tile
         int m_blk, n_begin, n_end;
-        unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+        unit_tiles<kEpi>(p, second ? u - units0 : u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk, ++tile_it) {
           const bool k_rev = p.k_serpentine && (tile_it & 1);
           for (int kq = 0; kq < k_stages; ++kq) {
@@ -284,15 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t sa = stage0 + stage * Cfg::kStageBytes + sub * Cfg::kSubBytes;
               const uint32_t sb = sa + Cfg::kABytes;
               if (!p.a_mn_major && p.a_kchunk) {
-                load3(sa, &tmA, am + p.a_mn0, (kx + p.a_k0) >> 6, pol_a);
+                load3(sa, &G.a, am + p.a_mn0, (kx + p.a_k0) >> 6, pol_a);
               } else if (!p.a_mn_major) {
-                load(sa, &tmA, kx + p.a_k0, am + p.a_mn0, pol_a);
+                load(sa, &G.a, kx + p.a_k0, am + p.a_mn0, pol_a);
               } else if (p.a_box3) {
-                load3(sa, &tmA, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
+                load3(sa, &G.a, kx + p.a_k0, (am + p.a_mn0) >> 6, pol_a);
               } else {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
-                  load(sa + j * kMnBoxBytes, &tmA, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
+                  load(sa + j * kMnBoxBytes, &G.a, am + 64 * j + p.a_mn0, kx + p.a_k0, pol_a);
               }
 #pragma unroll
               for (int h = 0; h < Cfg::kBHalves; ++h) {
@@ -300,13 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int bn = n_blk * Cfg::kTileN + h * BN + static_cast<int>(rank) * Cfg::kBRows;
                 const uint32_t sbh = sb + h * Cfg::kBHalfBytes;
                 if (!p.b_mn_major) {
-                  load(sbh, &tmB, kx + p.b_k0, bn + p.b_mn0, pol_b);
+                  load(sbh, &G.b, kx + p.b_k0, bn + p.b_mn0, pol_b);
                 } else if (p.b_box3) {
-                  load3(sbh, &tmB, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
+                  load3(sbh, &G.b, kx + p.b_k0, (bn + p.b_mn0) >> 6, pol_b);
                 } else {
 #pragma unroll
                   for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                    load(sbh + j * kMnBoxBytes, &tmB, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
+                    load(sbh + j * kMnBoxBytes, &G.b, bn + 64 * j + p.b_mn0, kx + p.b_k0, pol_b);
                 }
               }
             }
@@ -322,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        if (lane == 0) record_status(p.status, kStatusTimeout);
+        if (lane == 0) record_status(p0.status, kStatusTimeout);
         *abort_flag = 1;
       }
       // Drain before the final barrier. The even CTA waits for every stage phase it
@@ -352,13 +368,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued_any = false;
-      const bool a_mn = p.a_mn_major != 0, b_mn = p.b_mn_major != 0;
       int tile_it = 0;
-      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
+      for (int u = pair; ok && u < total_units; u += num_pairs) {
+        const bool second = kProducts == 2 && u >= units0;
+        const GemmParams& p = second ? g1.p : g0.p;
+        const int k_stages = (p.k_blocks + kSub - 1) / kSub;  // ring stages per tile
+        const int k_blocks = p.k_blocks;
+        const bool a_mn = p.a_mn_major != 0, b_mn = p.b_mn_major != 0;
+        const uint32_t idesc = p.idesc;
+        const bool serp = p.k_serpentine != 0;
         int m_blk, n_begin, n_end;
-        unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+        unit_tiles<kEpi>(p, second ? u - units0 : u, m_blk, n_begin, n_end);
         for (int n_blk = n_begin; ok && n_blk < n_end; ++n_blk, ++tile_it) {
-          const bool k_rev = p.k_serpentine && (tile_it & 1);
+          const bool k_rev = serp && (tile_it & 1);
           // both CTAs' epilogues must have drained this accumulator
           bool got;
           if constexpr (kCta == 2) {
@@ -386,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const int ks = k_rev ? k_stages - 1 - kq : kq;   // as the producer loaded it
-            const int nsub = min(kSub, p.k_blocks - ks * kSub);
+            const int nsub = min(kSub, k_blocks - ks * kSub);
             if (elect_one()) {
 #pragma unroll
             for (int sub = 0; sub < kSub; ++sub) {
@@ -404,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint64_t db = b_mn ? make_sw128_desc(sbh + k * (UK * 128), kMnBoxBytes, 1024)
                                            : make_sw128_desc(sbh + k * (UK * 2), 16, 1024);
                   const uint32_t dh = d_tmem + static_cast<uint32_t>(h * BN);
-                  if constexpr (kFp8) umma_f8_cg<kCta>(dh, da, db, p.idesc, accum);
-                  else umma_bf16_cg<kCta>(dh, da, db, p.idesc, accum);
+                  if constexpr (kFp8) umma_f8_cg<kCta>(dh, da, db, idesc, accum);
+                  else umma_bf16_cg<kCta>(dh, da, db, idesc, accum);
                 }
               }
             }
@@ -428,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        if (lane == 0) record_status(p.status, kStatusTimeout);
+        if (lane == 0) record_status(p0.status, kStatusTimeout);
         *abort_flag = 1;
       }
       if (issued_any) {
@@ -451,15 +473,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     float scale_v = 0.f;
-    if constexpr (kEpi == EPI_GRAD) scale_v = *p.scale;
+    if constexpr (kEpi == EPI_GRAD) scale_v = *p0.scale;
     float acc_scale = 1.f;  // FP8 operands: product of the two per-tensor scales
-    if constexpr (kFp8) acc_scale = *p.acc_scale_h * *p.acc_scale_w;
+    if constexpr (kFp8) acc_scale = *p0.acc_scale_h * *p0.acc_scale_w;
     // this warp's two staging boxes, used alternately
     const uint32_t stg = stage0 + Cfg::kRingBytes + static_cast<uint32_t>(quarter) * 2u * Cfg::kStgBytes;
     uint32_t nbox = 0;
-    for (int u = pair; ok && u < p.num_units; u += num_pairs) {
+    for (int u = pair; ok && u < total_units; u += num_pairs) {
+      const bool second = kProducts == 2 && u >= units0;
+      const GemmArgs& G = second ? g1 : g0;
+      const GemmParams& p = G.p;
       int m_blk, n_begin, n_end;
-      const int col_unit = unit_tiles<kEpi>(p, u, m_blk, n_begin, n_end);
+      const int col_unit = unit_tiles<kEpi>(p, second ? u - units0 : u, m_blk, n_begin, n_end);
       const int prow = m_blk * Cfg::kTileM + static_cast<int>(rank) * BM + row;  // product row
       const bool row_ok = prow < p.m_valid;
       int y = -1;
@@ -536,9 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               // rows and columns outside the map are dropped by the store
               const int oy = p.out_row0 + m_blk * Cfg::kTileM + static_cast<int>(rank) * BM +
                              quarter * 32;
-              if constexpr (kEpi == EPI_GRAD) tma_store_3d(&tmC, box, col & 63, oy, col >> 6);
-              else if (p.out_mode == OUT_ADD_F32) tma_reduce_add_2d(&tmC, box, col, oy);
-              else tma_store_2d(&tmC, box, col, oy);
+              if constexpr (kEpi == EPI_GRAD) tma_store_3d(&G.c, box, col & 63, oy, col >> 6);
+              else if (p.out_mode == OUT_ADD_F32) tma_reduce_add_2d(&G.c, box, col, oy);
+              else tma_store_2d(&G.c, box, col, oy);
               bulk_commit_group();
             }
             ++nbox;
@@ -566,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok) {
-      if (lane == 0) record_status(p.status, kStatusTimeout);
+      if (lane == 0) record_status(p0.status, kStatusTimeout);
       *abort_flag = 1;
     }
     // every store of this warp has landed before the CTA can exit
@@ -584,12 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Host-side launch of one instantiation: grid/kCta clusters of kCta CTAs, the tile
-// configuration's dynamic shared memory, the three tensor maps and the parameters
-// passed by value (the LSE epilogue ignores the output map c).
-template <int kEpi, int kCta, int kFp8, int kWide>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const GemmParams& p, int grid, cudaStream_t stream) {
-  auto kern = flce_gemm_kernel<kEpi, kCta, kFp8, kWide>;
+// configuration's dynamic shared memory, the products' maps and parameters passed
+// by value (g1 is ignored unless kProducts == 2).
+template <int kEpi, int kCta, int kFp8, int kWide, int kProducts = 1>
+cudaError_t launch_gemm(const GemmArgs& g0, const GemmArgs& g1, int grid, cudaStream_t stream) {
+  auto kern = flce_gemm_kernel<kEpi, kCta, kFp8, kWide, kProducts>;
   constexpr size_t smem = TileCfg<kCta, kWide>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -606,7 +630,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
+  return cudaLaunchKernelEx(&cfg, kern, g0, g1);
 }
 
 }  // namespace flce

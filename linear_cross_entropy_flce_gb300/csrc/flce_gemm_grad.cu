@@ -9,8 +9,13 @@ cudaError_t launch_gemm_grad(int cta_group, const CUtensorMap& a, const CUtensor
                              const CUtensorMap& c, const GemmParams& p, int grid,
                              cudaStream_t stream, int fp8) {
   if (cta_group != 2) return cudaErrorInvalidValue;  // only the pair kernel is built
-  return fp8 ? launch_gemm<EPI_GRAD, 2, 1, 0>(a, b, c, p, grid, stream)
-             : launch_gemm<EPI_GRAD, 2, 0, 0>(a, b, c, p, grid, stream);
+  GemmArgs g{};
+  g.a = a;
+  g.b = b;
+  g.c = c;
+  g.p = p;
+  return fp8 ? launch_gemm<EPI_GRAD, 2, 1, 0>(g, g, grid, stream)
+             : launch_gemm<EPI_GRAD, 2, 0, 0>(g, g, grid, stream);
 }
 
 }  // namespace flce

@@ -8,9 +8,12 @@ namespace flce {
 cudaError_t launch_gemm_lse(int cta_group, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t stream, int fp8) {
   if (cta_group != 2) return cudaErrorInvalidValue;  // only the pair kernel is built
-  const CUtensorMap unused = {};  // the LSE epilogue writes no tiles
-  return fp8 ? launch_gemm<EPI_LSE, 2, 1, 0>(a, b, unused, p, grid, stream)
-             : launch_gemm<EPI_LSE, 2, 0, 0>(a, b, unused, p, grid, stream);
+  GemmArgs g{};  // the LSE epilogue writes no tiles: no output map
+  g.a = a;
+  g.b = b;
+  g.p = p;
+  return fp8 ? launch_gemm<EPI_LSE, 2, 1, 0>(g, g, grid, stream)
+             : launch_gemm<EPI_LSE, 2, 0, 0>(g, g, grid, stream);
 }
 
 }  // namespace flce

@@ -2,6 +2,8 @@
 // shared with the host code that plans and launches it.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -123,6 +125,14 @@ struct GemmParams {
   // map is the chunk-major G, [columns/64][rows][64], boxes of 32 x 32 x 1.
   int out_row0;
   int out_mode;           // EPI_F32: OutMode (EPI_GRAD always stores bf16)
+};
+
+// Everything one product of a launch needs: the operand maps (A, B), the output
+// map of the epilogue's TMA stores (C; unused by the LSE epilogue) and the
+// parameters. A launch carries one or two of them (flce_gemm_kernel kProducts).
+struct GemmArgs {  // aligned as CUtensorMap (128 bytes)
+  CUtensorMap a, b, c;
+  GemmParams p;
 };
 
 }  // namespace flce

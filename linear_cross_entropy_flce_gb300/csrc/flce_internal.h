@@ -28,6 +28,12 @@ cudaError_t launch_gemm_f32(int cta_group, const CUtensorMap& a, const CUtensorM
                             const CUtensorMap& c, const GemmParams& p, int grid,
                             cudaStream_t stream, int wide);
 
+// Two products of 256 x 512 tiles and the fp32 epilogue in one launch: the units of
+// `first` (its p.num_units) are dealt to the pairs before those of `second`. Both
+// only read what earlier launches wrote, and their outputs do not overlap.
+cudaError_t launch_gemm_f32_pair(int cta_group, const GemmArgs& first, const GemmArgs& second,
+                                 int grid, cudaStream_t stream);
+
 // Per-token merge of the vocabulary-range partials into lse and the per-token
 // negative log-likelihood.
 // part is [splits][part_stride][128] (max, sum exp) pairs.
