@@ -429,6 +429,58 @@ def run_ce_logits(args, wl, world, rank, local):
     return 0
 
 
+def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -> dict:
+    """The roofline block of the JSON line from the per-kernel CUDA-event times.
+
+    kernel_ms: ms per step of each kernel kind; n_kind / per_kind: launches and
+    total ms of each kind over `steps` traced steps. The dominant kernel is the
+    tcgen05 GEMM with the fp32 epilogue, whose one launch per chunk computes both
+    dW = G^T H and dH = G W (two 2 N c D products): half of the step's flops and
+    the largest time share. The kernels are timed as launches inside a step well
+    under a second long, so the burst cuBLAS peak is the denominator; the
+    sustained one is reported beside it. Every fraction is a quotient of the
+    block's own numbers and the peaks."""
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
+    gemm_flops = 2.0 * N * V * D   # per step, for each of the four products
+
+    def rate(ms_per_step):
+        return gemm_flops / (ms_per_step / 1e3) / 1e12 if ms_per_step > 0 else None
+
+    mult = {"dwdh_gemm": 2.0}
+    f32_ms = kernel_ms["dwdh_gemm"]
+    f32_launches = n_kind["dwdh_gemm"]
+    achieved = 2.0 * gemm_flops / (f32_ms / 1e3) / 1e12
+    products = {}
+    for name, k in (("lse", "lse_gemm"), ("gradient", "grad_gemm"), ("dW + dH", "dwdh_gemm")):
+        r = mult.get(k, 1.0) * rate(kernel_ms[k])
+        products[name] = {"kernel": k, "tflops": r, "frac": r / burst,
+                          "frac_of_sustained": r / sustained}
+    total = sum(kernel_ms.values())
+    return {
+        "bound": "tensor", "unit": "TFLOP/s",
+        "kernel": "flce_gemm_kernel<EPI_F32> (tcgen05, 256 x 512 tiles: dW = G^T H and dH = G W, one launch per chunk)",
+        "achieved": achieved, "peak": burst, "frac": achieved / burst,
+        "peak_kind": f"bf16 cuBLAS burst, {peaks.get('source', 'measured')} (MEASURED_PEAKS.json bf16_tflops)",
+        "peak_sustained": sustained, "frac_of_sustained": achieved / sustained,
+        "products": products,
+        "launches_per_step": f32_launches // steps,
+        "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / steps),
+        "ms_per_launch_avg": per_kind["dwdh_gemm"] / max(f32_launches, 1),
+        "traffic": traffic,
+        "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
+                          "dram__bytes_write.sum per launch; null if the kernel changed)",
+        "kernel_sha": kernel_source_sha(),
+        "kernels": {k: {"ms_per_step": kernel_ms[k],
+                        "ms_per_launch": per_kind[k] / max(n_kind[k], 1),
+                        "launches_per_step": n_kind[k] // steps,
+                        "tflops": mult.get(k, 1.0) * rate(kernel_ms[k]) if k.endswith("gemm") else None,
+                        "share": kernel_ms[k] / total}
+                    for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dwdh_gemm",
+                              "dh_round"] if k in kernel_ms},
+    }
+
+
 def config_block(wl, world) -> dict:
     return {"workload": f"{wl.name}: FLCE head N={wl.N} tokens, D={wl.D}, V={wl.V}, "
                         f"labels {wl.labels}, {int(round(wl.p_ignore * 100))}% ignore_index=-100",
@@ -610,7 +662,6 @@ def main(argv=None) -> int:
             per_kind[kinds[k]] += evs[k].elapsed_time(evs[k + 1])
             n_kind[kinds[k]] += 1
     kernel_ms = {k: per_kind[k] / args.steps for k in per_kind}      # per step
-    kernel_launch_ms = {k: per_kind[k] / max(n_kind[k], 1) for k in per_kind}
     quant_ms = None
     if fp8 is not None:   # the two device quantisations of a step, timed alone
         torch.cuda.synchronize(dev)
@@ -690,47 +741,10 @@ def main(argv=None) -> int:
     value = N * world / (ms / 1e3)
     burst = peaks["bf16_tflops"]
     sustained = peaks.get("bf16_tflops_sustained", burst)
-    gemm_flops = 2.0 * N * V * D   # per step, for each of the four products
-
-    def rate(ms_per_step):
-        return gemm_flops / (ms_per_step / 1e3) / 1e12 if ms_per_step > 0 else None
-
-    # The dominant kernel: the tcgen05 GEMM with the fp32 epilogue, whose one launch
-    # per chunk computes both dW = G^T H and dH = G W: half of the step's flops and
-    # the largest time share. The kernels are timed as launches inside a step well
-    # under a second long, so the burst cuBLAS peak is the denominator; the
-    # sustained one is reported beside it.
-    f32_ms = kernel_ms["dwdh_gemm"]
-    f32_launches = n_kind["dwdh_gemm"]
-    achieved = 2.0 * gemm_flops / (f32_ms / 1e3) / 1e12
-    products = {}
-    for name, k, mult in (("lse", "lse_gemm", 1.0), ("gradient", "grad_gemm", 1.0),
-                          ("dW + dH", "dwdh_gemm", 2.0)):
-        r = mult * rate(kernel_ms[k])
-        products[name] = {"kernel": k, "tflops": r, "frac": r / burst,
-                          "frac_of_sustained": r / sustained}
-    roofline = {
-        "bound": "tensor", "unit": "TFLOP/s",
-        "kernel": "flce_gemm_kernel<EPI_F32> (tcgen05, 256 x 512 tiles: dW = G^T H and dH = G W, one launch per chunk)",
-        "achieved": achieved, "peak": burst, "frac": achieved / burst,
-        "peak_kind": f"bf16 cuBLAS burst, {peaks['source']} (MEASURED_PEAKS.json bf16_tflops)",
-        "peak_sustained": sustained, "frac_of_sustained": achieved / sustained,
-        "products": products,
-        "launches_per_step": f32_launches // args.steps,
-        "flops_per_launch_avg": 2.0 * gemm_flops / (f32_launches / args.steps),
-        "ms_per_launch_avg": per_kind["dwdh_gemm"] / max(f32_launches, 1),
-        "traffic": measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name, plan["v_chunk"]),
-        "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
-                          "dram__bytes_write.sum per launch; null if the kernel changed)",
-        "kernel_sha": kernel_source_sha(),
-        "kernels": {k: {"ms_per_step": kernel_ms[k], "ms_per_launch": kernel_launch_ms[k],
-                        "launches_per_step": n_kind[k] // args.steps,
-                        "tflops": ((2.0 if k == "dwdh_gemm" else 1.0) * rate(kernel_ms[k])
-                                   if k.endswith("gemm") else None),
-                        "share": kernel_ms[k] / sum(kernel_ms.values())}
-                    for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dwdh_gemm",
-                              "dh_round"] if k in kernel_ms},
-    }
+    roofline = make_roofline(N, V, D, kernel_ms, n_kind, per_kind, args.steps, peaks,
+                             measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name,
+                                              plan["v_chunk"]))
+    products = roofline["products"]
     clocks = clk.summary()
 
     cpu = None
