@@ -70,6 +70,25 @@ def test_wide_dw_tile_edges(N, D, V, opts):
     _run_and_compare(Hb, Wb, y, **opts)
 
 
+@pytest.mark.parametrize("N,D,V", [(200, 16384, 3000), (300, 8200, 2000)])
+def test_large_hidden_sizes(N, D, V):
+    """Hidden sizes of the largest heads: D = 16384 (256 K blocks in the logits
+    products, 32 wide dW tiles across D), and D = 8200, not a multiple of 64 (the
+    MN-major H and W operands of dW and dH then load as two 2-D boxes per half)."""
+    Hb, Wb, y = _inputs(N, D, V, seed=D, w_std=0.01, p_ignore=0.05)
+    _run_and_compare(Hb, Wb, y)
+
+
+def test_one_label_for_every_token():
+    """Every valid token has the same label: dW row y sums 1900 one-hot terms of
+    -scale h_i, so its softmax part is about 1e-4 of the row and only the fp32
+    accumulation allowance of the gate separates rounding from error there; every
+    other row is all softmax part."""
+    Hb, Wb, y = _inputs(2000, 256, 3000, seed=26, p_ignore=0.05)
+    y[y != -100] = 7
+    _run_and_compare(Hb, Wb, y)
+
+
 def test_labels_at_vocabulary_edges():
     Hb, Wb, y = _inputs(256, 128, 1000, seed=5)
     y[:64] = 0
