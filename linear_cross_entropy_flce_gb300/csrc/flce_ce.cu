@@ -54,6 +54,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Element-wise maximum of two bf16 pairs (exact); -inf in both halves.
+constexpr uint32_t kBf16NegInf2 = 0xFF80FF80u;
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // 16-byte vector of logits: 4 fp32 or 8 bf16, widened to fp32.
 template <int kBf16>
 struct Vec16;
@@ -400,6 +408,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const float scale = kGrad ? *scale_ptr : 0.f;
+  const float log2_abs_scale = kGrad && kBf16 ? log2f(fabsf(scale)) : 0.f;  // -inf for 0
   const int nvec = V / E;
   const int crank = static_cast<int>(cta_rank_in_cluster());
   const int csize = static_cast<int>(ctas_in_cluster());
@@ -455,9 +464,36 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
                                       static_cast<uint64_t>(timeout_ns)))
       timed_out = true;
     const uint8_t* sl = buf[b];
-    // pass 1: running max and sum of exponentials over the staged slice
+    // pass 1: max and sum of exponentials over the staged slice
     float m = -INFINITY, s = 0.f;
-    {
+    if constexpr (kBf16) {
+      // The thread's maximum first, two elements per packed compare (exact on
+      // bf16), then the sum of exponentials against that one maximum: a second
+      // read of shared memory instead of an fp32 compare and a running rescale
+      // per element.
+      uint32_t pm0 = kBf16NegInf2, pm1 = kBf16NegInf2;
+#pragma unroll 4
+      for (int v = tid; v < nv; v += kCeThreads) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+        pm0 = bf16x2_max(pm0, bf16x2_max(w.x, w.y));
+        pm1 = bf16x2_max(pm1, bf16x2_max(w.z, w.w));
+      }
+      pm0 = bf16x2_max(pm0, pm1);
+      m = fmaxf(bf16_lo(pm0), bf16_hi(pm0));
+      if (m != -INFINITY) {
+        const float ms = m * kLog2e;
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 2
+        for (int v = tid; v < nv; v += kCeThreads) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+          acc0 += ex2a(fmaf(bf16_lo(w.x), kLog2e, -ms)) + ex2a(fmaf(bf16_hi(w.x), kLog2e, -ms));
+          acc1 += ex2a(fmaf(bf16_lo(w.y), kLog2e, -ms)) + ex2a(fmaf(bf16_hi(w.y), kLog2e, -ms));
+          acc0 += ex2a(fmaf(bf16_lo(w.z), kLog2e, -ms)) + ex2a(fmaf(bf16_hi(w.z), kLog2e, -ms));
+          acc1 += ex2a(fmaf(bf16_lo(w.w), kLog2e, -ms)) + ex2a(fmaf(bf16_hi(w.w), kLog2e, -ms));
+        }
+        s = acc0 + acc1;
+      }
+    } else {
       constexpr int kU = 2;
       int v = tid;
       for (; v + (kU - 1) * kCeThreads < nv; v += kU * kCeThreads) {
@@ -465,13 +501,8 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v + u * kCeThreads) * 16);
-          if constexpr (kBf16) {
-            x[u][0] = bf16_lo(w.x); x[u][1] = bf16_hi(w.x); x[u][2] = bf16_lo(w.y); x[u][3] = bf16_hi(w.y);
-            x[u][4] = bf16_lo(w.z); x[u][5] = bf16_hi(w.z); x[u][6] = bf16_lo(w.w); x[u][7] = bf16_hi(w.w);
-          } else {
-            x[u][0] = __uint_as_float(w.x); x[u][1] = __uint_as_float(w.y);
-            x[u][2] = __uint_as_float(w.z); x[u][3] = __uint_as_float(w.w);
-          }
+          x[u][0] = __uint_as_float(w.x); x[u][1] = __uint_as_float(w.y);
+          x[u][2] = __uint_as_float(w.z); x[u][3] = __uint_as_float(w.w);
         }
         float cm = m;
 #pragma unroll
@@ -492,13 +523,8 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
       for (; v < nv; v += kCeThreads) {
         const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
         float x[E];
-        if constexpr (kBf16) {
-          x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-          x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-        } else {
-          x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
-          x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
-        }
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
         float cm = m;
 #pragma unroll
         for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[e]);
@@ -581,25 +607,44 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
       const float sc = y >= 0 ? scale : 0.f;
       const float nl2 = -lse * kLog2e;
       uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
-      for (int v = tid; v < nv; v += kCeThreads) {
-        const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
-        float x[E];
-        if constexpr (kBf16) {
-          x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-          x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-        } else {
-          x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
-          x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
-        }
+      if constexpr (kBf16) {
+        // |scale| folded into the exponent, 2^(z log2e - lse log2e + log2|scale|),
+        // and its sign applied to the packed bf16 pair: no multiply per element.
+        // An ignored token's exponent is -inf, so its row is zeros.
+        const float nl2s = (y >= 0 ? log2_abs_scale : -INFINITY) + nl2;
+        const float asc = fabsf(sc);
+        const uint32_t sgn = sc < 0.f ? 0x80008000u : 0u;
+        for (int v = tid; v < nv; v += kCeThreads) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+          float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                        bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
-        const int base = (v0 + v) * E;
-        if (static_cast<unsigned>(y - base) < static_cast<unsigned>(E)) {
+          for (int e = 0; e < 8; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2s));
+          const int base = (v0 + v) * 8;
+          if (static_cast<unsigned>(y - base) < 8u) {
 #pragma unroll
-          for (int e = 0; e < E; ++e)
-            if (base + e == y) x[e] -= sc;
+            for (int e = 0; e < 8; ++e)
+              if (base + e == y) x[e] -= asc;
+          }
+          *reinterpret_cast<uint4*>(gr + static_cast<int64_t>(v0 + v) * 16) =
+              make_uint4(pack_bf16(x[0], x[1]) ^ sgn, pack_bf16(x[2], x[3]) ^ sgn,
+                         pack_bf16(x[4], x[5]) ^ sgn, pack_bf16(x[6], x[7]) ^ sgn);
         }
-        VT::store(gr + static_cast<int64_t>(v0 + v) * 16, x);
+      } else {
+        for (int v = tid; v < nv; v += kCeThreads) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
+          float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                        __uint_as_float(w.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
+          const int base = (v0 + v) * 4;
+          if (static_cast<unsigned>(y - base) < 4u) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (base + e == y) x[e] -= sc;
+          }
+          VT::store(gr + static_cast<int64_t>(v0 + v) * 16, x);
+        }
       }
       if (last) {
         for (int i = nvec * E + tid; i < V; i += kCeThreads) {

@@ -56,7 +56,7 @@ def _check(res, ref, grad=True, per_token=False, y=None, opts=None):
             onehot = np.zeros(r.shape, dtype=bool)
             rows = np.nonzero(np.asarray(y) != (opts or {}).get("ignore_index", -100))[0]
             onehot[rows, np.asarray(y)[rows]] = True
-            sc = float(grad_scale_f32(ref["n_valid"], opts))
+            sc = abs(float(grad_scale_f32(ref["n_valid"], opts)))
             rho = (2.0 ** -8 if res.dlogits.dtype == torch.bfloat16 else 2.0 ** -22) + 2e-3
             bound = rho * (np.abs(r) + 2.0 * sc * onehot) + 1e-37
             worst = float(np.max(np.abs(d - r) / bound))
@@ -98,6 +98,26 @@ def test_reductions_and_scales(opts):
     Z, y, t, lab = _logits(150, 2048, seed=42, p_ignore=0.2)
     res = flce.ce_logits(t, lab, **opts)
     _check(res, oracle.ce_logits(Z, y, **opts), y=y, opts=opts)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("grad_scale", [-2.5, 0.75])
+def test_staged_rows_with_scales_and_ignored_tokens(bf16, grad_scale):
+    """Rows long enough for the shared-memory staged kernel (bf16: 131 KB rows,
+    fp32: 262 KB rows, both on clusters of 3 CTAs), a fifth of the tokens ignored,
+    and a negative or fractional upstream gradient scale: the bf16 gradient pass
+    takes the scale's magnitude into the exponent and applies its sign to the
+    packed result, so both signs are checked element by element."""
+    N, V = 48, 65600
+    ld = (V + 7) // 8 * 8
+    Z, y, t, lab = _logits(N, V, seed=47 + int(bf16), bf16=bf16, ld=ld, p_ignore=0.2)
+    opts = {"grad_scale": grad_scale}
+    res = flce.ce_logits(t, lab, **opts)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    _check(res, oracle.ce_logits(Z, y, **opts), y=y, opts=opts)
+    ignored = torch.from_numpy(y == -100).to(t.device)
+    assert int(ignored.sum()) > 0
+    assert torch.count_nonzero(res.dlogits[ignored]).item() == 0
 
 
 def test_per_token_losses_forward_only():
