@@ -10,9 +10,10 @@
 //   3. reduce     n_valid, label check, loss, gradient scale (one block, fixed order)
 //   4. for each token block b, for each vocabulary chunk c:
 //        GRAD GEMM  recompute Z_bc, write G_bc = (softmax - onehot) * scale in bf16
-//        dW GEMM    dW_c  (+)= G_bc^T H_b   (fixed order over token blocks)
-//        dH GEMM    dH_b  (+)= G_bc W_c     (fp32 accumulator; the last chunk
-//                   rounds to bf16)              (same page, 2.)
+//        dH + dW    one launch of both products (same page, 2.):
+//                   dH_b  (+)= G_bc W_c     (fp32 accumulator over the chunks)
+//                   dW_c  (+)= G_bc^T H_b   (fixed order over token blocks)
+//      then, with several chunks, the rounding of the block's dH accumulator to bf16
 // Nothing of size N x V is ever written: the largest buffer is one G chunk.
 // flce_forward runs steps 1-3. On one vocabulary shard, flce_forward_shard runs
 // step 1 with global label ids, a merge into the shard's (m, s, zt) and step 3
