@@ -99,6 +99,7 @@ def test_labels_at_vocabulary_edges():
 @pytest.mark.parametrize("opts", [
     {"reduction": "sum"},
     {"grad_scale": 0.25},
+    {"grad_scale": -1.5},   # a negative upstream factor flips every gradient's sign
     {"normalizer": 1000.0},
     {"ignore_index": 7},
 ])
