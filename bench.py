@@ -429,6 +429,143 @@ def run_ce_logits(args, wl, world, rank, local):
     return 0
 
 
+OTHER_WORKLOADS = ("llama2", "qwen2_7b", "long_seq")
+
+
+def time_steps(step, steps, stream, dev, local, flush=None) -> dict:
+    """Device time of `steps` calls of step(), each bracketed by its own CUDA events
+    on `stream`; with `flush` (a device buffer larger than L2) the buffer is
+    overwritten before every step, outside the events, so each step starts with
+    cold L2."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            if flush is not None:
+                flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    times = sorted(a.elapsed_time(b) for a, b in evs)
+    c = clk.summary()
+    return {"ms_per_step": sum(times) / steps, "ms_median": times[len(times) // 2],
+            "steps": steps, "sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
+
+
+def other_workloads(args, flce, H, W, lab, wl_main, dev, local, stream, peaks) -> dict:
+    """The 'workloads' block of the default line: every other head of the
+    benchmark set (forward + backward, default plan), and the Llama-3-8B head's
+    forward-only and FP8 steps, each timed in this run. The heads' inputs are
+    drawn by the same seeded recipe; L2 is flushed before every timed step. An
+    entry that fails records its error instead of stopping the run."""
+    import torch
+    burst = peaks["bf16_tflops"]
+    steps, warmup = max(1, args.other_steps), 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
+    block = {"note": ("each entry timed in this run after the main measurement: seeded "
+                      "inputs by the same recipe, default plan, CUDA events per step on the "
+                      "launching stream, L2 flushed (256 MB written) before every step")}
+
+    def check(status):
+        code = flce.check_status(status, stream.cuda_stream)
+        if code != flce.FLCE_OK:
+            raise RuntimeError(f"device status {code}: {flce.status_string(code)}")
+
+    for name in OTHER_WORKLOADS:
+        try:
+            wl = flce_inputs.get(name)
+            Hb, Wb, y = flce_inputs.make_inputs(wl)
+            Hx = torch.from_numpy(Hb.view(np.int16)).to(dev).view(torch.bfloat16)
+            Wx = torch.from_numpy(Wb.view(np.int16)).to(dev).view(torch.bfloat16)
+            lx = torch.from_numpy(y).to(dev)
+            del Hb, Wb
+            N, D, V = wl.N, wl.D, wl.V
+            ws_bytes = flce.workspace_size(N, D, V)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+                   "lse": torch.empty(N, dtype=torch.float32, device=dev),
+                   "dH": torch.empty(N, D, dtype=torch.bfloat16, device=dev),
+                   "dW": torch.empty(V, D, dtype=torch.float32, device=dev)}
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def step():
+                flce.forward_backward(Hx, Wx, lx, out=out, workspace=ws, status=status,
+                                      stream=stream.cuda_stream)
+            for _ in range(warmup):
+                step()
+            check(status)
+            t = time_steps(step, steps, stream, dev, local, flush)
+            check(status)
+            tf = 8.0 * N * V * D / (t["ms_per_step"] * 1e-3) / 1e12
+            block[name] = {"workload": config_block(wl, 1)["workload"], **t,
+                           "tokens_per_s": N / (t["ms_per_step"] * 1e-3), "tflops_8nvd": tf,
+                           "frac_of_burst_bf16": tf / burst, "workspace_bytes": ws_bytes,
+                           "logits_bytes_unfused": N * V * 4}
+            del Hx, Wx, lx, ws, out
+        except Exception as e:   # keep the main line
+            block[name] = {"error": str(e)[:300]}
+
+    N, D, V = wl_main.N, wl_main.D, wl_main.V
+    try:   # forward only (loss and lse), the evaluation path
+        ws = torch.empty(flce.forward_workspace_size(N, D, V), dtype=torch.uint8, device=dev)
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(N, dtype=torch.float32, device=dev)}
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def fstep():
+            flce.forward(H, W, lab, out=out, workspace=ws, status=status,
+                         stream=stream.cuda_stream)
+        for _ in range(warmup):
+            fstep()
+        check(status)
+        t = time_steps(fstep, steps, stream, dev, local, flush)
+        check(status)
+        tf = 2.0 * N * V * D / (t["ms_per_step"] * 1e-3) / 1e12
+        block[f"{wl_main.name}_forward_only"] = {
+            **t, "tokens_per_s": N / (t["ms_per_step"] * 1e-3), "tflops_2nvd": tf,
+            "frac_of_burst_bf16": tf / burst, "workspace_bytes": ws.numel()}
+        del ws, out
+    except Exception as e:
+        block[f"{wl_main.name}_forward_only"] = {"error": str(e)[:300]}
+
+    try:   # E4M3 logits products, H and W quantised on the device every step
+        q = (torch.empty(N, D, dtype=torch.uint8, device=dev),
+             torch.empty(2, dtype=torch.float32, device=dev),
+             torch.empty(V, D, dtype=torch.uint8, device=dev),
+             torch.empty(2, dtype=torch.float32, device=dev))
+        ws = torch.empty(flce.workspace_size(N, D, V), dtype=torch.uint8, device=dev)
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(N, dtype=torch.float32, device=dev),
+               "dH": torch.empty(N, D, dtype=torch.bfloat16, device=dev),
+               "dW": torch.empty(V, D, dtype=torch.float32, device=dev)}
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def qstep():
+            flce.quantize_e4m3(H, q=q[0], out=q[1], stream=stream.cuda_stream)
+            flce.quantize_e4m3(W, q=q[2], out=q[3], stream=stream.cuda_stream)
+            flce.forward_backward_fp8(q[0], q[1], q[2], q[3], lab, H, W, out=out, workspace=ws,
+                                      status=status, stream=stream.cuda_stream)
+        for _ in range(warmup):
+            qstep()
+        check(status)
+        t = time_steps(qstep, steps, stream, dev, local, flush)
+        check(status)
+        block[f"{wl_main.name}_fp8"] = {
+            **t, "tokens_per_s": N / (t["ms_per_step"] * 1e-3),
+            "tflops_8nvd_effective": 8.0 * N * V * D / (t["ms_per_step"] * 1e-3) / 1e12,
+            "note": "E4M3 logits products (forward, recompute), bf16 dH and dW products; "
+                    "each step quantises H and W on the device first"}
+        del q, ws, out
+    except Exception as e:
+        block[f"{wl_main.name}_fp8"] = {"error": str(e)[:300]}
+    del flush
+    torch.cuda.empty_cache()
+    return block
+
+
 def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -> dict:
     """The roofline block of the JSON line from the per-kernel CUDA-event times.
 
@@ -515,6 +652,11 @@ def main(argv=None) -> int:
                          "logits products, bf16 H and W for the gradient products")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the 'workloads' block (the other heads, forward only, FP8) "
+                         "that the default Llama-3-8B run adds to its line")
+    ap.add_argument("--other-steps", type=int, default=10,
+                    help="timed steps per entry of the 'workloads' block")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -763,6 +905,11 @@ def main(argv=None) -> int:
                              f"float64 flops)"},
                "tiny_single_core": oracle_tiny_single_core()}
 
+    others = None
+    if (rank == 0 and world == 1 and fp8 is None and not args.no_other_workloads
+            and wl.name == "llama3_8b"):
+        others = other_workloads(args, flce, H, W, lab, wl, dev, local, stream, peaks)
+
     if fp8 is not None:
         # the two logits products run on E4M3 operands: their denominator is cuBLASLt's
         # own E4M3 GEMM (torch._scaled_mm) timed in this process at the LSE product's
@@ -799,6 +946,8 @@ def main(argv=None) -> int:
         "gpu_launches": (plan["kernel_launches"] + (4 if fp8 is not None else 0)) * args.steps,
         "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
     }
+    if others is not None:
+        line["workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     rep.close()
