@@ -167,7 +167,10 @@ def test_matches_fused_loss_on_the_same_logits():
 
 @pytest.mark.parametrize("N,V,bf16", [
     (40, 128256, False),   # 501 KB rows: staged slices, cluster of 5
-    (24, 128257, True),    # 250 KB bf16 rows with a scalar tail: staged, cluster of 3
+    (24, 128257, True),    # 250 KB bf16 rows with a scalar tail: staged, cluster of 5
+    (1000, 65600, True),   # bf16, cluster of 3, about 10 rows per cluster: both buffers
+                           # and both exchange slots reused many times
+    (400, 128257, True),   # bf16 with a tail, cluster of 5, about 7 rows per cluster
     (9, 100003, False),    # staged (cluster of 4), ragged fp32 tail
     (4, 240007, False),    # 938 KB rows: streamed kernel, cluster of 4
 ])
