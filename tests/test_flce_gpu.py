@@ -89,6 +89,22 @@ def test_one_label_for_every_token():
     _run_and_compare(Hb, Wb, y)
 
 
+@pytest.mark.parametrize("opts", [{}, {"v_splits": 3}])
+def test_peaked_logits_online_lse(opts):
+    """Logits with a standard deviation of about 30 (the online maximum jumps by
+    tens between vocabulary tiles, and each row's softmax is close to one-hot),
+    half of the labels on the row's largest logit (p close to 1, so the target
+    entry of G is a difference of nearly equal numbers) and half uniform (p close
+    to 0)."""
+    Hb, Wb, y = _inputs(300, 256, 3000, seed=31, w_std=0.5, h_scale=4.0, p_ignore=0.05)
+    Z = flce_inputs.bf16_bits_to_f64(Hb) @ flce_inputs.bf16_bits_to_f64(Wb).T
+    assert Z.std() > 20.0
+    top = np.argmax(Z, axis=1).astype(np.int32)
+    half = np.arange(len(y)) % 2 == 0
+    y = np.where((y != -100) & half, top, y).astype(np.int32)
+    _run_and_compare(Hb, Wb, y, **opts)
+
+
 def test_labels_at_vocabulary_edges():
     Hb, Wb, y = _inputs(256, 128, 1000, seed=5)
     y[:64] = 0

@@ -64,6 +64,21 @@ def test_result_at_the_stated_precision_passes():
     assert_within(errs)
 
 
+def test_peaked_logits_at_the_stated_precision_pass():
+    """The gates hold for the GPU test of peaked logits (std about 30, half of the
+    labels on the row's largest logit): a result at the stated precision passes."""
+    wl = flce_inputs.Workload("custom", 300, 256, 3000, 4.0, 0.5, "uniform", 0.05, seed=31)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H = flce_inputs.bf16_bits_to_f64(Hb)
+    W = flce_inputs.bf16_bits_to_f64(Wb)
+    top = np.argmax(H @ W.T, axis=1).astype(np.int32)
+    half = np.arange(len(y)) % 2 == 0
+    y = np.where((y != -100) & half, top, y).astype(np.int32)
+    ref = oracle.flce(H, W, y, want_abs=True)
+    errs = _errs(H, W, y, ref, _host_result(H, W, y, ref))
+    assert_within(errs)
+
+
 def test_softmax_part_twenty_percent_off_is_caught():
     H, W, y, ref = _case()
     errs = _errs(H, W, y, ref, _host_result(H, W, y, ref, softmax_factor=0.8))
