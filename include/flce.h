@@ -114,7 +114,8 @@ void flce_default_options(flce_options* opt);
  * Bytes of device workspace that flce_forward_backward and flce_forward need for
  * this problem and these options (opt may be NULL for the defaults). The
  * workspace holds the per-(token, vocabulary range) partial max/sum-exp pairs,
- * the target logits, one bf16 chunk of G ([n_block, v_chunk]) and, when the
+ * the target logits, per token the (max, 1 / sum, 1 - p of the target) the
+ * gradient is formed from (16 bytes), one bf16 chunk of G ([n_block, v_chunk]) and, when the
  * vocabulary spans several chunks, an fp32 [n_block, D] dH accumulator (plus an
  * fp32 [V, D] dW accumulator only for bf16 dW with several token blocks). It is
  * the whole extra device memory of a call and is far below the N*V*4 bytes of

@@ -187,8 +187,8 @@ struct Plan {
   int64_t n_block = 0, v_chunk = 0;
   int n_nblocks = 0, n_chunks = 0;
   bool need_dh_acc = false, need_dw_acc = false;
-  size_t off_part = 0, off_zt = 0, off_nll = 0, off_lse = 0, off_scal = 0, off_g = 0,
-         off_dhacc = 0, off_dwacc = 0, total = 0;
+  size_t off_part = 0, off_zt = 0, off_nll = 0, off_lse = 0, off_scal = 0, off_gstat = 0,
+         off_g = 0, off_dhacc = 0, off_dwacc = 0, total = 0;
 };
 
 int choose_splits(int m_blocks, int v_tiles, int sms) {
@@ -264,11 +264,12 @@ int make_plan(int64_t N, int64_t D, int64_t V, const flce_options& o, int sms, P
   p.off_lse = take(static_cast<size_t>(N) * 4);
   p.off_scal = take(256);
   if (backward) {
+    p.off_gstat = take(static_cast<size_t>(N) * 16);   // float4 per token
     p.off_g = take(static_cast<size_t>(rows_b) * cv * 2);
     p.off_dhacc = p.need_dh_acc ? take(static_cast<size_t>(rows_b) * D * 4) : off;
     p.off_dwacc = p.need_dw_acc ? take(static_cast<size_t>(V) * D * 4) : off;
   } else {
-    p.off_g = p.off_dhacc = p.off_dwacc = off;
+    p.off_gstat = p.off_g = p.off_dhacc = p.off_dwacc = off;
   }
   p.total = off;
   *P = p;
@@ -408,6 +409,9 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
   float* lse = lse_out ? lse_out : reinterpret_cast<float*>(ws + P.off_lse);
   float* scal = reinterpret_cast<float*>(ws + P.off_scal);  // [0] scale
   int32_t* nvalid = reinterpret_cast<int32_t*>(ws + P.off_scal + 4);
+  // per token (max, 1 / sum exp, 1 - p of the target) for the gradient epilogue;
+  // a shard's backward has only the caller's combined lse
+  float4* gstat = (backward && !shard) ? reinterpret_cast<float4*>(ws + P.off_gstat) : nullptr;
   uint16_t* G = reinterpret_cast<uint16_t*>(ws + P.off_g);
   float* dh_acc = reinterpret_cast<float*>(ws + P.off_dhacc);
   float* dw_acc = reinterpret_cast<float*>(ws + P.off_dwacc);
@@ -479,7 +483,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
                                    static_cast<int>(v_base + V), P.part_stride, P.splits,
                                    o.ignore_index, sh.m, sh.s, sh.zt, st)
               : launch_lse_merge(part, zt, labels, static_cast<int>(N), static_cast<int>(V),
-                                 P.part_stride, P.splits, o.ignore_index, lse, nll, st);
+                                 P.part_stride, P.splits, o.ignore_index, lse, nll, gstat, st);
     if (me != cudaSuccess || !trace()) return FLCE_ERR_CUDA;
   }
   // ---- 3. reduce: label check, n, the gradient scale and (not for shards) the loss ----
@@ -543,6 +547,7 @@ int run(const uint16_t* H, const uint16_t* W, const Fp8Operands& f8, const int32
       q.col_base = static_cast<int>(v_base + c0);
       q.ignore_index = o.ignore_index;
       q.lse = lse_g;
+      q.gstat = gstat;
       q.scale = scal;
       q.out_row0 = 0;
       if (launch_gemm_grad(cta, mH_k, mW_k, mG_out, q, cta * std::min(q.num_units, pairs), st,

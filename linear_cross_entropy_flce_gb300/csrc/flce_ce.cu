@@ -314,13 +314,12 @@ __global__ void __launch_bounds__(kCeThreads)
       const float lse = s_lse;
       const int y = s_y;
       const float sc = y >= 0 ? scale : 0.f;
-      const float nl2 = -lse * kLog2e;
       uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
       for (int w = v0 + tid; w < v1; w += kCeThreads) {
         float x[E];
         VT::load(zr + static_cast<int64_t>(w) * 16, x);
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
+        for (int e = 0; e < E; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
         const int base = w * E;
         if (static_cast<unsigned>(y - base) < static_cast<unsigned>(E)) {
 #pragma unroll
@@ -331,7 +330,7 @@ __global__ void __launch_bounds__(kCeThreads)
       }
       if (last) {
         for (int i = nvec * E + tid; i < V; i += kCeThreads) {
-          float x = ex2a(fmaf(VT::load1(zr + static_cast<int64_t>(i) * kElt), kLog2e, nl2)) * sc;
+          float x = ex2a((VT::load1(zr + static_cast<int64_t>(i) * kElt) - lse) * kLog2e) * sc;
           if (i == y) x -= sc;
           VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
         }
@@ -408,7 +407,6 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const float scale = kGrad ? *scale_ptr : 0.f;
-  const float log2_abs_scale = kGrad && kBf16 ? log2f(fabsf(scale)) : 0.f;  // -inf for 0
   const int nvec = V / E;
   const int crank = static_cast<int>(cta_rank_in_cluster());
   const int csize = static_cast<int>(ctas_in_cluster());
@@ -605,30 +603,25 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
       const float lse = s_lse;
       const int y = s_y;
       const float sc = y >= 0 ? scale : 0.f;
-      const float nl2 = -lse * kLog2e;
       uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
+      // exponent (z - lse) * log2 e, the difference first: exact when z is close to
+      // lse, so a confident target keeps p - 1 to about an fp32 ulp
       if constexpr (kBf16) {
-        // |scale| folded into the exponent, 2^(z log2e - lse log2e + log2|scale|),
-        // and its sign applied to the packed bf16 pair: no multiply per element.
-        // An ignored token's exponent is -inf, so its row is zeros.
-        const float nl2s = (y >= 0 ? log2_abs_scale : -INFINITY) + nl2;
-        const float asc = fabsf(sc);
-        const uint32_t sgn = sc < 0.f ? 0x80008000u : 0u;
         for (int v = tid; v < nv; v += kCeThreads) {
           const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
           float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                         bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2s));
+          for (int e = 0; e < 8; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
           const int base = (v0 + v) * 8;
           if (static_cast<unsigned>(y - base) < 8u) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              if (base + e == y) x[e] -= asc;
+              if (base + e == y) x[e] -= sc;
           }
           *reinterpret_cast<uint4*>(gr + static_cast<int64_t>(v0 + v) * 16) =
-              make_uint4(pack_bf16(x[0], x[1]) ^ sgn, pack_bf16(x[2], x[3]) ^ sgn,
-                         pack_bf16(x[4], x[5]) ^ sgn, pack_bf16(x[6], x[7]) ^ sgn);
+              make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                         pack_bf16(x[6], x[7]));
         }
       } else {
         for (int v = tid; v < nv; v += kCeThreads) {
@@ -636,7 +629,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
           float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                         __uint_as_float(w.w)};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nl2)) * sc;
+          for (int e = 0; e < 4; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
           const int base = (v0 + v) * 4;
           if (static_cast<unsigned>(y - base) < 4u) {
 #pragma unroll
@@ -648,7 +641,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
       }
       if (last) {
         for (int i = nvec * E + tid; i < V; i += kCeThreads) {
-          float x = ex2a(fmaf(VT::load1(zr + static_cast<int64_t>(i) * kElt), kLog2e, nl2)) * sc;
+          float x = ex2a((VT::load1(zr + static_cast<int64_t>(i) * kElt) - lse) * kLog2e) * sc;
           if (i == y) x -= sc;
           VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
         }

@@ -78,13 +78,16 @@ __device__ __forceinline__ void record_status(int32_t* status, int code) {
 // ---- epilogue bodies ---------------------------------------------------------------
 
 struct LseState {
-  float m;   // running max of z
-  float s;   // running sum of exp(z - m)
+  float m;   // running max of z (the target's logit included)
+  float s;   // running sum of exp(z - m) over every column but the target's
   float zt;  // target logit
   bool found;
 };
 
-// One 32-column chunk of the logits tile for this thread's row.
+// One 32-column chunk of the logits tile for this thread's row. The target's own
+// term is left out of the sum (the merge adds it back), so that 1 - p of the
+// target, the sum of the other terms over the whole sum, is known without a
+// difference of nearly equal numbers.
 __device__ __forceinline__ void lse_chunk(const float (&v)[32], int col_local, int n_valid,
                                           int rel_target, LseState& st) {
   float x[32];
@@ -95,12 +98,6 @@ __device__ __forceinline__ void lse_chunk(const float (&v)[32], int col_local, i
     for (int k = 0; k < 32; ++k)
       if (col_local + k >= n_valid) x[k] = -INFINITY;
   }
-  if (static_cast<unsigned>(rel_target) < 32u) {
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (k == rel_target) st.zt = v[k];
-    st.found = true;
-  }
   float c0 = fmaxf(x[0], x[1]), c1 = fmaxf(x[2], x[3]);
 #pragma unroll
   for (int k = 4; k < 32; k += 4) {
@@ -108,6 +105,15 @@ __device__ __forceinline__ void lse_chunk(const float (&v)[32], int col_local, i
     c1 = fmaxf(c1, fmaxf(x[k + 2], x[k + 3]));
   }
   const float mn = fmaxf(st.m, fmaxf(c0, c1));
+  if (static_cast<unsigned>(rel_target) < 32u) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k == rel_target) {
+        st.zt = v[k];
+        x[k] = -INFINITY;   // in the max above, not in the sum below
+      }
+    st.found = true;
+  }
   if (mn == -INFINITY) return;
   const float ms = mn * kLog2e;
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
@@ -147,15 +153,20 @@ __device__ __forceinline__ void stage_bf16_row(uint32_t box, int r, const float 
                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
 
-// G for one 32-column chunk: (exp(z - lse) - [v = y]) * sc, 0 past n_valid.
+// G for one 32-column chunk: (exp(z - zmax) * a - [v = y] * sc, 0 past n_valid,
+// with a = sc / sum exp(z - zmax) (or zmax = lse and a = sc). The exponent's
+// difference is taken first, exact when z is close to zmax. The target entry is
+// -sc * q with q = 1 - p as the merge formed it, when q >= 0 is given; else
+// (a vocabulary shard, which has only lse) exp(z - lse) * sc - sc.
 __device__ __forceinline__ void grad_chunk(const float (&v)[32], int col_local, int n_valid,
-                                           int rel_target, float nlse2, float sc, float (&g)[32]) {
+                                           int rel_target, float zmax, float a, float sc,
+                                           float q, float (&g)[32]) {
 #pragma unroll
-  for (int k = 0; k < 32; ++k) g[k] = ex2_approx(fmaf(v[k], kLog2e, nlse2)) * sc;
+  for (int k = 0; k < 32; ++k) g[k] = ex2_approx((v[k] - zmax) * kLog2e) * a;
   if (static_cast<unsigned>(rel_target) < 32u) {
 #pragma unroll
     for (int k = 0; k < 32; ++k)
-      if (k == rel_target) g[k] -= sc;
+      if (k == rel_target) g[k] = q >= 0.f ? -sc * q : g[k] - sc;
   }
   if (col_local + 32 > n_valid) {
 #pragma unroll
@@ -495,13 +506,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       LseState st{-INFINITY, 0.f, 0.f, false};
-      // Rows past the product (or of another token block) get exponent -inf, so
+      // Rows past the product (or of another token block) take zmax = +inf, so
       // their G is exactly 0 whatever logits the tile holds for them.
-      float nlse2 = -INFINITY, sc = 0.f;
+      float zmax = INFINITY, a = 0.f, sc = 0.f, q = -1.f;
       if constexpr (kEpi == EPI_GRAD) {
         if (row_ok) {
-          nlse2 = -p.lse[p.row_base + prow] * kLog2e;
           sc = (y >= 0) ? scale_v : 0.f;
+          if (p.gstat != nullptr) {
+            const float4 gs = p.gstat[p.row_base + prow];
+            zmax = gs.x;
+            a = sc * gs.y;
+            q = gs.z;
+          } else {
+            zmax = p.lse[p.row_base + prow];
+            a = sc;
+          }
         }
       }
       for (int n_blk = n_begin; n_blk < n_end; ++n_blk) {
@@ -548,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if constexpr (kEpi == EPI_GRAD) {
               float g[32];
-              grad_chunk(v, col, p.n_valid, y - (p.col_base + col), nlse2, sc, g);
+              grad_chunk(v, col, p.n_valid, y - (p.col_base + col), zmax, a, sc, q, g);
               stage_bf16_row(box, lane, g);
             } else if (p.out_mode == OUT_STORE_BF16) {
               stage_bf16_row(box, lane, v);

@@ -118,7 +118,11 @@ struct GemmParams {
   int ignore_index;
   float2* part;           // EPI_LSE: [splits][part_stride][BM] (max, sum exp)
   float* zt;              // EPI_LSE: target logit per token
-  const float* lse;       // EPI_GRAD: lse[row_base + row]
+  const float* lse;       // EPI_GRAD: lse[row_base + row] (used when gstat is null)
+  // EPI_GRAD: per token (max of z, 1 / sum exp(z - max), 1 - p of the target, 0):
+  // G = exp(z - max) / sum * scale, and the target entry -scale * (1 - p) taken as
+  // it is, with no difference of nearly equal numbers when p is close to 1
+  const float4* gstat;
   const float* scale;     // EPI_GRAD: device scalar grad_scale / n
   // EPI_F32: the output map (third tensor map) holds product row r at map row
   // out_row0 + r, product column c at map column c; boxes of 32 x 32. EPI_GRAD: the

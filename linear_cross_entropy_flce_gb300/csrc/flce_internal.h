@@ -35,11 +35,13 @@ cudaError_t launch_gemm_f32_pair(int cta_group, const GemmArgs& first, const Gem
                                  int grid, cudaStream_t stream);
 
 // Per-token merge of the vocabulary-range partials into lse and the per-token
-// negative log-likelihood.
-// part is [splits][part_stride][128] (max, sum exp) pairs.
+// negative log-likelihood, and (gstat not null) per token (max, 1 / sum exp,
+// 1 - p of the target, 0) for the gradient epilogue.
+// part is [splits][part_stride][128] (max, sum exp over every id but the target's)
+// pairs; zt holds the target logits.
 cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
                              int V, int part_stride, int splits, int ignore_index, float* lse,
-                             float* nll, cudaStream_t stream);
+                             float* nll, float4* gstat, cudaStream_t stream);
 
 // Vocabulary shard [v_lo, v_hi): per token the shard's max m, sum of exp(z - m)
 // and the target logit when the label lies in the shard (else 0).

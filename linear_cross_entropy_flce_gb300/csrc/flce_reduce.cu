@@ -21,24 +21,35 @@ __device__ __forceinline__ float ex2f_approx(float x) {
   return y;
 }
 
+// The partial sums leave out the target's own term (LSE epilogue), so per token
+//   S_o = sum over the other ids of exp(z - M),  e_t = exp(z_target - M),
+//   lse = M + log(S_o + e_t),  NLL = log(1 + S_o / e_t),  1 - p = S_o / (S_o + e_t),
+// none of them a difference of nearly equal numbers when p is close to 1. With
+// gstat, (M, 1 / S, 1 - p, 0) is stored for the gradient epilogue.
 __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
                                  const int32_t* __restrict__ labels, int N, int V, int part_stride,
                                  int splits, int ignore_index, float* __restrict__ lse,
-                                 float* __restrict__ nll) {
+                                 float* __restrict__ nll, float4* __restrict__ gstat) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int r = i / BM, l = i - (i / BM) * BM;
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, part[(static_cast<int64_t>(s) * part_stride + r) * BM + l].x);
-  float S = 0.f;
+  float So = 0.f;
   for (int s = 0; s < splits; ++s) {
     const float2 pr = part[(static_cast<int64_t>(s) * part_stride + r) * BM + l];
-    S += pr.y * ex2f_approx((pr.x - M) * kLog2e);
+    So += pr.y * ex2f_approx((pr.x - M) * kLog2e);
   }
+  const int y = labels[i];
+  const bool valid = y != ignore_index && y >= 0 && y < V;
+  const float zy = valid ? zt[i] : -INFINITY;
+  const float et = valid ? ex2f_approx((zy - M) * kLog2e) : 0.f;
+  const float S = So + et;
   const float L = M + logf(S);
   lse[i] = L;
-  const int y = labels[i];
-  nll[i] = (y != ignore_index && y >= 0 && y < V) ? L - zt[i] : 0.f;
+  // e_t = 0: the target is so far below the max that lse - z_t has no cancellation
+  nll[i] = !valid ? 0.f : (et > 0.f ? log1pf(So / et) : L - zy);
+  if (gstat != nullptr) gstat[i] = make_float4(M, 1.f / S, So / S, 0.f);
 }
 
 // One vocabulary shard (ids [v_lo, v_hi) of a vocabulary split over several
@@ -60,10 +71,13 @@ __global__ void shard_merge_kernel(const float2* __restrict__ part, const float*
     const float2 pr = part[(static_cast<int64_t>(s) * part_stride + r) * BM + l];
     S += pr.y * ex2f_approx((pr.x - M) * kLog2e);
   }
+  const int y = labels[i];
+  const bool here = y != ignore_index && y >= v_lo && y < v_hi;
+  // the partial sums leave out the target's term: the shard's sum includes it
+  if (here) S += ex2f_approx((zt[i] - M) * kLog2e);
   m_out[i] = M;
   s_out[i] = S;
-  const int y = labels[i];
-  zt_out[i] = (y != ignore_index && y >= v_lo && y < v_hi) ? zt[i] : 0.f;
+  zt_out[i] = here ? zt[i] : 0.f;
 }
 
 constexpr int kReduceThreads = 1024;
@@ -303,10 +317,10 @@ cudaError_t launch_scale(void* x, int64_t bytes, int bf16, const float* scale, i
 
 cudaError_t launch_lse_merge(const float2* part, const float* zt, const int32_t* labels, int N,
                              int V, int part_stride, int splits, int ignore_index, float* lse,
-                             float* nll, cudaStream_t stream) {
+                             float* nll, float4* gstat, cudaStream_t stream) {
   const int threads = 256;
   lse_merge_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(
-      part, zt, labels, N, V, part_stride, splits, ignore_index, lse, nll);
+      part, zt, labels, N, V, part_stride, splits, ignore_index, lse, nll, gstat);
   return cudaGetLastError();
 }
 

@@ -13,9 +13,14 @@ Gates (each written out in assert_within):
     or h_i (dW row y_i). From the oracle the exact c_i is removed; from the GPU
     result the value that the precision reading admits for that entry: G is
     rounded once to bf16 from its fp32 value, and at the target that rounding is
-    as large as the whole softmax part of a row. What is left compares
+    as large as the whole softmax part of a row. The fused path forms that fp32
+    value as -scale * (1 - p) from the forward merge's 1 - p (no cancellation
+    when p is close to 1); a vocabulary shard's backward, which has only lse, as
+    p * scale - scale. What is left compares
     sum over non-target entries of g_iv x: relative Frobenius <= 5e-3 over the
-    rows (per group of dW ids at full size), <= 2e-2 per row. Outputs rounded to
+    rows (per group of dW ids at full size), <= 2e-2 per row (plus 1e-6 of the
+    largest row: a row whose whole gradient is below that, a token so confident
+    that its gradient is about 1e-17, is zero at the output's precision). Outputs rounded to
     bf16 (dH always, dW on request) add their own rounding, whose root-mean-square
     is at most 2^-8/sqrt(3) of the output's norm; that amount is added to the
     bound (aggregate and per row). So is the fp32 accumulation of sums that the
@@ -48,6 +53,9 @@ U_BF16 = 2.0 ** -8                 # unit roundoff of bfloat16 (8 significant bi
 NOISE_BF16 = U_BF16 / np.sqrt(3.0)  # upper estimate of the rms relative rounding error
 ACC_F32 = 2.0 ** -22                # per sqrt(addition): fp32 accumulation noise allowance
 RHO = U_BF16 + 2e-3 + 1e-3
+# per-row gates: rows whose whole gradient is below 1e-6 of the largest row are
+# zero at the output's precision (the element-wise bound has the same floor)
+ROW_FLOOR = 1e-6
 IGNORE_INDEX = -100
 
 
@@ -96,20 +104,34 @@ def _bf16_round(x32: np.ndarray) -> np.ndarray:
     return flce_inputs.bf16_bits_to_f64(flce_inputs.f32_to_bf16_bits(np.asarray(x32, dtype=np.float32)))
 
 
-def target_terms(nll: np.ndarray, valid: np.ndarray, scale32: np.float32, scale64: float):
+def target_terms(nll: np.ndarray, valid: np.ndarray, scale32: np.float32, scale64: float,
+                 form: str = "ratio"):
     """Per token: the oracle's target entry c = scale * (p - 1) with p = exp(-nll),
-    and the bf16 value(s) the GPU's G can hold there: fl32(fl32(p * s) - s) rounded
-    once to bf16. Where a relative error of 1e-4 in p or two fp32 ulps of s could
-    move the fp32 value across a bf16 rounding boundary, both neighbours are
-    admissible (alt is NaN elsewhere). Ignored tokens: 0."""
-    p = np.exp(-np.asarray(nll, dtype=np.float64))
+    and the bf16 value(s) the GPU's G can hold there, rounded once to bf16 from
+    its fp32 value. form "ratio" (the fused path, which keeps 1 - p = q from the
+    forward merge): fl32(-s * fl32(q)); form "lse" (a vocabulary shard's backward,
+    which has only lse): fl32(fl32(p * s) - s). Where a relative error of 1e-4 in
+    q (or p) or two fp32 ulps of s could move the fp32 value across a bf16
+    rounding boundary, both neighbours are admissible (alt is NaN elsewhere).
+    Ignored tokens: 0."""
+    nll = np.asarray(nll, dtype=np.float64)
+    p = np.exp(-nll)
     s32 = np.float32(scale32)
     c_exact = np.where(valid, scale64 * (p - 1.0), 0.0)
-    ulp = np.float64(np.spacing(s32))
-    x = p * np.float64(s32)
-    mid = np.float32(np.float32(np.float32(p) * s32) - s32)
-    lo = np.float32((x * (1.0 + 1e-4)) - np.float64(s32) - 2.0 * ulp)
-    hi = np.float32((x * (1.0 - 1e-4)) - np.float64(s32) + 2.0 * ulp)
+    if form == "ratio":
+        q = -np.expm1(-nll)                      # 1 - p without cancellation
+        x = q * np.float64(s32)
+        mid = np.float32(-np.float64(np.float32(q)) * np.float64(s32))
+        lo = np.float32(-x * (1.0 + 1e-4) - 2.0 * np.spacing(np.float32(x)))
+        hi = np.float32(-x * (1.0 - 1e-4) + 2.0 * np.spacing(np.float32(x)))
+    elif form == "lse":
+        ulp = np.float64(np.spacing(s32))
+        x = p * np.float64(s32)
+        mid = np.float32(np.float32(np.float32(p) * s32) - s32)
+        lo = np.float32((x * (1.0 + 1e-4)) - np.float64(s32) - 2.0 * ulp)
+        hi = np.float32((x * (1.0 - 1e-4)) - np.float64(s32) + 2.0 * ulp)
+    else:
+        raise ValueError(form)
     c_gpu = _bf16_round(mid)
     b_lo, b_hi = _bf16_round(lo), _bf16_round(hi)
     alt = np.where(b_lo != c_gpu, b_lo, np.where(b_hi != c_gpu, b_hi, np.nan))
@@ -145,7 +167,7 @@ def _ratio(num, den):
 
 
 def compare(res, ref, dh_rows=None, dw_rows=None, *, labels=None, Hg=None, Wg=None, opts=None,
-            dh_f32=False, dw_groups=None) -> dict:
+            dh_f32=False, dw_groups=None, target_form="ratio") -> dict:
     """Errors of a GPU result against the oracle's.
 
     res: the binding's result (loss, lse, dH, dW tensors); ref: oracle.flce(...),
@@ -154,7 +176,8 @@ def compare(res, ref, dh_rows=None, dw_rows=None, *, labels=None, Hg=None, Wg=No
     labels, Hg, Wg (host arrays: the gradient operands, float32 or float64) and
     opts (reduction, grad_scale, normalizer, ignore_index, dw_dtype) enable the
     softmax-part gates. dh_f32: dH is fp32 (not rounded to bf16). dw_groups maps a
-    name to positions in ref["dw_rows"] that are gated separately."""
+    name to positions in ref["dw_rows"] that are gated separately. target_form:
+    how the GPU formed G's target entry (target_terms)."""
     o = opts or {}
     ignore = o.get("ignore_index", IGNORE_INDEX)
     dw_bf16 = o.get("dw_dtype") == "bfloat16"
@@ -169,7 +192,7 @@ def compare(res, ref, dh_rows=None, dw_rows=None, *, labels=None, Hg=None, Wg=No
         valid = y != ignore
         s32 = grad_scale_f32(ref["n_valid"], o)
         s64 = _scale64(ref["n_valid"], o)
-        c_exact, c_gpu, c_alt = target_terms(ref["nll"], valid, s32, s64)
+        c_exact, c_gpu, c_alt = target_terms(ref["nll"], valid, s32, s64, target_form)
         yc = np.where(valid, y, 0)
 
     if getattr(res, "dH", None) is not None and ref["dH"] is not None:
@@ -190,7 +213,9 @@ def compare(res, ref, dh_rows=None, dw_rows=None, *, labels=None, Hg=None, Wg=No
             out["dH_soft"] = _ratio(float(np.linalg.norm(delta)),
                                     TOL_SOFT_FRO * float(np.linalg.norm(t_ref)) + nu)
             dn = np.linalg.norm(delta, axis=1)
-            den = TOL_SOFT_ROW * np.linalg.norm(t_ref, axis=1) + noise * np.linalg.norm(dref, axis=1)
+            rn = np.linalg.norm(dref, axis=1)
+            den = (TOL_SOFT_ROW * np.linalg.norm(t_ref, axis=1) + noise * rn
+                   + ROW_FLOOR * float(rn.max(initial=0.0)))
             live = den > 0
             out["dH_soft_row"] = float(np.max(dn[live] / den[live])) if np.any(live) else 0.0
             if np.any(~live & (dn > 0)):
@@ -232,7 +257,9 @@ def compare(res, ref, dh_rows=None, dw_rows=None, *, labels=None, Hg=None, Wg=No
                 out["dW_soft" + sfx] = _ratio(float(np.linalg.norm(delta[g])),
                                               TOL_SOFT_FRO * float(np.linalg.norm(t_ref[g])) + nu)
                 dn = np.linalg.norm(delta[g], axis=1)
-                den = TOL_SOFT_ROW * np.linalg.norm(t_ref[g], axis=1) + noise * np.linalg.norm(dref[g], axis=1)
+                rn = np.linalg.norm(dref[g], axis=1)
+                den = (TOL_SOFT_ROW * np.linalg.norm(t_ref[g], axis=1) + noise * rn
+                       + ROW_FLOOR * float(rn.max(initial=0.0)))
                 live = den > 0
                 r = float(np.max(dn[live] / den[live])) if np.any(live) else 0.0
                 out["dW_soft_row" + sfx] = float("inf") if np.any(~live & (dn > 0)) else r

@@ -36,14 +36,21 @@ def _bf16(x):
 
 
 def _host_result(H, W, y, ref, softmax_factor=1.0, target_shift=0):
-    """loss, lse, dH (bf16) and dW (fp32) with G = bf16(fl32(p * s) - s * onehot)."""
+    """loss, lse, dH (bf16) and dW (fp32) with G = bf16(fl32(p * s)) off the target
+    and bf16(fl32(-s * fl32(1 - p))) at it, as the fused path forms them. A
+    target_shift plants the one-hot term in another column (subtracted there, the
+    true target left at p * s)."""
     valid = y != -100
     s = np.float32(1.0 / valid.sum())
     p = np.exp(H @ W.T - ref["lse"][:, None]) * softmax_factor
     G = (p.astype(np.float32) * s).astype(np.float32)
     rows = np.nonzero(valid)[0]
     cols = (y[rows] + target_shift) % W.shape[0]
-    G[rows, cols] = (G[rows, cols] - s).astype(np.float32)
+    if target_shift == 0:
+        q = (-np.expm1(-ref["nll"][rows])).astype(np.float32)   # 1 - p of the target
+        G[rows, cols] = (-np.float64(s) * q.astype(np.float64)).astype(np.float32)
+    else:
+        G[rows, cols] = (G[rows, cols] - s).astype(np.float32)
     G[~valid] = 0.0
     Gb = _bf16(G)
     dH = _bf16((Gb @ W).astype(np.float32))
