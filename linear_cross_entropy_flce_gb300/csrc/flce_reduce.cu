@@ -23,7 +23,8 @@ __device__ __forceinline__ float ex2f_approx(float x) {
 
 // The partial sums leave out the target's own term (LSE epilogue), so per token
 //   S_o = sum over the other ids of exp(z - M),  e_t = exp(z_target - M),
-//   lse = M + log(S_o + e_t),  NLL = log(1 + S_o / e_t),  1 - p = S_o / (S_o + e_t),
+//   lse = M + log(S_o + e_t),  NLL = log(1 + S_o / e_t) (lse - z_t once e_t < 2^-60),
+//   1 - p = S_o / (S_o + e_t),
 // none of them a difference of nearly equal numbers when p is close to 1. With
 // gstat, (M, 1 / S, 1 - p, 0) is stored for the gradient epilogue.
 __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ zt,
@@ -47,8 +48,9 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   const float S = So + et;
   const float L = M + logf(S);
   lse[i] = L;
-  // e_t = 0: the target is so far below the max that lse - z_t has no cancellation
-  nll[i] = !valid ? 0.f : (et > 0.f ? log1pf(So / et) : L - zy);
+  // e_t < 2^-60 (the target more than 41 below the max): lse - z_t has no
+  // cancellation, and S_o / e_t, with S_o at most V < 2^30, cannot overflow above it
+  nll[i] = !valid ? 0.f : (et >= 0x1p-60f ? log1pf(So / et) : L - zy);
   if (gstat != nullptr) gstat[i] = make_float4(M, 1.f / S, So / S, 0.f);
 }
 

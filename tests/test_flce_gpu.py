@@ -105,6 +105,26 @@ def test_peaked_logits_online_lse(opts):
     _run_and_compare(Hb, Wb, y, **opts)
 
 
+def test_targets_far_below_a_flat_maximum():
+    """Most logits of a row equal (the maximum shared by about 2950 ids) and the
+    target 70-86 below it: the target's term is a normal fp32 number far smaller
+    than the sum of the others, whose ratio to it would overflow fp32 (the loss
+    must stay finite and equal the oracle's)."""
+    N, D, V = 128, 64, 3000
+    H = np.zeros((N, D), dtype=np.float32)
+    H[:, 0] = 10.0
+    H[:, 1] = np.linspace(-1.0, 1.0, N, dtype=np.float32)
+    W = np.zeros((V, D), dtype=np.float32)
+    W[:, 0] = 1.0
+    targets = np.arange(50)
+    W[targets, 0] = -7.5 + 0.02 * targets.astype(np.float32)   # z about -75 .. -65
+    y = (np.arange(N) % 50).astype(np.int32)
+    y[::17] = -100
+    Hb, Wb = flce_inputs.f32_to_bf16_bits(H), flce_inputs.f32_to_bf16_bits(W)
+    res, ref = _run_and_compare(Hb, Wb, y)
+    assert np.isfinite(float(res.loss.item())) and ref["loss"] > 70.0
+
+
 def test_labels_at_vocabulary_edges():
     Hb, Wb, y = _inputs(256, 128, 1000, seed=5)
     y[:64] = 0
