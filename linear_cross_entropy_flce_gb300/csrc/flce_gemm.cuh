@@ -2,14 +2,15 @@
 // epilogues. Every product of fused linear cross-entropy runs through it:
 //
 //   LSE  : Z = H W^T tile by tile, accumulated in TMEM; the epilogue keeps a
-//          per-token running max and sum of exponentials across the vocabulary
-//          tiles of a work unit and extracts the target logit ("Liger Kernel:
-//          Fused Triton Kernels for LLM Training", The Architecture, 1. steps
-//          2-5: in-SRAM tile product, online LogSumExp, immediate target
-//          extraction, no logits written).
+//          per-token running max and sum of exponentials (the target's own term
+//          left out) across the vocabulary tiles of a work unit and extracts the
+//          target logit ("Liger Kernel: Fused Triton Kernels for LLM Training",
+//          The Architecture, 1. steps 2-5: in-SRAM tile product, online
+//          LogSumExp, immediate target extraction, no logits written).
 //   GRAD : Z recomputed tile by tile; the epilogue forms
-//          G = (exp(z - lse) - [v = y]) * scale in bf16 and writes one chunk of G,
-//          stored chunk-major (same page, 2. In-Kernel Gradient Computation:
+//          G = (exp(z - lse) - [v = y]) * scale in bf16, as exp(z - max) * scale /
+//          sum off the target and -scale * (1 - p) at it, and writes one chunk of
+//          G, stored chunk-major (same page, 2. In-Kernel Gradient Computation:
 //          recompute the tile logits from the saved LSE, derive dL/dz in the kernel).
 //   F32  : plain product whose tile is stored as fp32, added to fp32 already in
 //          memory, or stored as bf16 — used for dW = G^T H and dH = G W (same
