@@ -108,6 +108,40 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mn;
 }
 
+// A row's merged (max M, sum S_o of exp(z - M) over every id but the target's,
+// target logit z_t) to what the gradient pass and the loss need, with no
+// difference of nearly equal numbers when p of the target is close to 1.
+// row_grad, before the gradient pass: e_t = exp(z_t - M), S = S_o + e_t, and
+// dZ = exp(z - M) * a off the target, -scale * q at it, with a = scale / S and
+// q = S_o / S (1 - p). row_loss, after it (only the CTA that writes the loss):
+// lse = M + log S and NLL = log1p(S_o / e_t), or lse - z_t once e_t < 2^-60,
+// where that has no cancellation and S_o / e_t could overflow.
+struct RowStat {
+  float M, So, zt, et, S, a, q;
+  bool valid;
+};
+
+__device__ __forceinline__ RowStat row_grad(float M, float So, float zt, bool valid,
+                                            float scale) {
+  RowStat r;
+  r.M = M;
+  r.So = So;
+  r.zt = zt;
+  r.valid = valid;
+  r.et = valid ? ex2a((zt - M) * kLog2e) : 0.f;
+  r.S = So + r.et;
+  float inv;   // S >= 1 (the row's maximum term is 1): the hardware reciprocal, within 1 ulp
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(r.S));
+  r.a = (valid ? scale : 0.f) * inv;
+  r.q = So * inv;
+  return r;
+}
+
+__device__ __forceinline__ void row_loss(const RowStat& r, float& lse, float& nll) {
+  lse = r.M + logf(r.S);
+  nll = !r.valid ? 0.f : (r.et >= 0x1p-60f ? log1pf(r.So / r.et) : lse - r.zt);
+}
+
 __global__ void __launch_bounds__(kCountThreads)
     ce_count_kernel(const int32_t* __restrict__ labels, int N, int V, int ignore_index,
                     int reduction, float grad_scale, float normalizer, float* scale,
@@ -203,7 +237,7 @@ __global__ void __launch_bounds__(kCeThreads)
   constexpr int kUnroll = 32 / E;  // 32 values (8 or 4 16-byte loads) in flight per thread
   __shared__ float2 s_red[kCeThreads / 32];
   __shared__ float2 s_part[2];  // this CTA's (max, sum exp), alternating between rows
-  __shared__ float s_lse;
+  __shared__ float s_zmax, s_a, s_q;  // the row's max, scale / sum, 1 - p of the target
   __shared__ int s_y;  // target id, -1 when the token is ignored
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -218,10 +252,15 @@ __global__ void __launch_bounds__(kCeThreads)
   const bool last = crank == csize - 1;        // also owns the scalar tail
 
   int it = 0;
+  int yl_next = cluster < N ? labels[cluster] : 0;  // each row's label is read a row ahead
   for (int row = cluster; row < N; row += nclusters, ++it) {
     const uint8_t* zr = z + static_cast<int64_t>(row) * ld_bytes;
+    const int yl = yl_next;
+    if (row + nclusters < N) yl_next = labels[row + nclusters];
+    const int yt = (yl != ignore_index && yl >= 0 && yl < V) ? yl : -1;  // target, or -1
     float m = -INFINITY, s = 0.f;
-    // pass 1: running max and sum of exponentials over this CTA's slice
+    // pass 1: running max (the target included) and sum of exponentials (the
+    // target's term left out) over this CTA's slice
     int v = v0 + tid;
     for (; v + (kUnroll - 1) * kCeThreads < v1; v += kUnroll * kCeThreads) {
       float x[kUnroll][E];
@@ -233,6 +272,15 @@ __global__ void __launch_bounds__(kCeThreads)
       for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
         for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[u][e]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int base = (v + u * kCeThreads) * E;
+        if (static_cast<unsigned>(yt - base) < static_cast<unsigned>(E)) {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (base + e == yt) x[u][e] = -INFINITY;
+        }
+      }
       const float ms = cm * kLog2e;
       float acc = 0.f;
 #pragma unroll
@@ -248,6 +296,12 @@ __global__ void __launch_bounds__(kCeThreads)
       float cm = m;
 #pragma unroll
       for (int e = 0; e < E; ++e) cm = fmaxf(cm, x[e]);
+      const int base = v * E;
+      if (static_cast<unsigned>(yt - base) < static_cast<unsigned>(E)) {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (base + e == yt) x[e] = -INFINITY;
+      }
       const float ms = cm * kLog2e;
       float acc = 0.f;
 #pragma unroll
@@ -258,7 +312,7 @@ __global__ void __launch_bounds__(kCeThreads)
     if (last) {
       for (int i = nvec * E + tid; i < V; i += kCeThreads) {
         const float x = VT::load1(zr + static_cast<int64_t>(i) * kElt);
-        lse_merge(m, s, x, 1.f);
+        lse_merge(m, s, x, i == yt ? 0.f : 1.f);
       }
     }
     // block merge: warp shuffles, then the first warp
@@ -284,59 +338,59 @@ __global__ void __launch_bounds__(kCeThreads)
     }
     // The target logit is read before the cluster barrier: after it, peers may
     // overwrite their slices with the gradient (in place).
-    int y = -1;
-    bool valid = false;
     float zt = 0.f;
-    if (tid == 0) {
-      y = labels[row];
-      valid = y != ignore_index && y >= 0 && y < V;
-      if (crank == 0 && valid) zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
-    }
+    if (tid == 0 && yt >= 0) zt = VT::load1(zr + static_cast<int64_t>(yt) * kElt);
     // cluster merge through distributed shared memory
     cluster_barrier();
+    RowStat rs;
     if (tid == 0) {
       float M = -INFINITY, S = 0.f;
       for (int r = 0; r < csize; ++r) {
         const float2 pr = ld_dsmem_f2(&s_part[it & 1], static_cast<uint32_t>(r));
         lse_merge(M, S, pr.x, pr.y);
       }
-      const float lse = M + logf(S);
-      if (crank == 0) {
-        if (lse_out != nullptr) lse_out[row] = lse;
-        nll_out[row] = valid ? lse - zt : 0.f;
-      }
-      s_lse = lse;
-      s_y = valid ? y : -1;
+      rs = row_grad(M, S, zt, yt >= 0, scale);
+      s_zmax = M;
+      s_a = rs.a;
+      s_q = rs.q;
+      s_y = yt;
     }
     __syncthreads();
+    if (tid == 0 && crank == 0) {  // the loss, off the gradient pass's critical path
+      float lse, nll;
+      row_loss(rs, lse, nll);
+      if (lse_out != nullptr) lse_out[row] = lse;
+      nll_out[row] = nll;
+    }
     if constexpr (kGrad) {
-      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale over this CTA's slice
-      const float lse = s_lse;
+      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale over this CTA's slice, as
+      // exp(z - M) * scale / S off the target and -scale * (1 - p) at it
+      const float zmax = s_zmax, a = s_a;
       const int y = s_y;
-      const float sc = y >= 0 ? scale : 0.f;
+      const float gt = y >= 0 ? -scale * s_q : 0.f;
       uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
       for (int w = v0 + tid; w < v1; w += kCeThreads) {
         float x[E];
         VT::load(zr + static_cast<int64_t>(w) * 16, x);
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
+        for (int e = 0; e < E; ++e) x[e] = ex2a((x[e] - zmax) * kLog2e) * a;
         const int base = w * E;
         if (static_cast<unsigned>(y - base) < static_cast<unsigned>(E)) {
 #pragma unroll
           for (int e = 0; e < E; ++e)
-            if (base + e == y) x[e] -= sc;
+            if (base + e == y) x[e] = gt;
         }
         VT::store(gr + static_cast<int64_t>(w) * 16, x);
       }
       if (last) {
         for (int i = nvec * E + tid; i < V; i += kCeThreads) {
-          float x = ex2a((VT::load1(zr + static_cast<int64_t>(i) * kElt) - lse) * kLog2e) * sc;
-          if (i == y) x -= sc;
+          float x = ex2a((VT::load1(zr + static_cast<int64_t>(i) * kElt) - zmax) * kLog2e) * a;
+          if (i == y) x = gt;
           VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
         }
       }
     }
-    __syncthreads();  // s_red, s_lse, s_y are reused by the next row
+    __syncthreads();  // s_red and the row's values in shared memory are reused
   }
   // No CTA leaves while a peer may still read its s_part through the cluster.
   cluster_barrier();
@@ -402,7 +456,10 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   __shared__ __align__(8) uint64_t s_xbar[2];
   __shared__ __align__(16) float4 s_msg[2][kMaxCeCluster];
   __shared__ float2 s_red[kCeThreads / 32];
-  __shared__ float s_lse;
+  // the row's -max * log2 e, that plus log2 |scale / sum| (bf16 rows), scale / sum and
+  // 1 - p of the target
+  __shared__ float s_nm2, s_c, s_a, s_q;
+  __shared__ float s_zt;  // the target logit, when it lies in this CTA's slice
   __shared__ int s_y;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -452,6 +509,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
   int row = cluster;
   if (tid == 0 && row < N && nv > 0) issue(row, 0);
   bool timed_out = false;
+  int yl_next = row < N ? labels[row] : 0;  // each row's label is read a row ahead
   for (; row < N; row += nclusters, ++it) {
     const int b = it & 1;
     const uint8_t* zr = z + static_cast<int64_t>(row) * ld_bytes;
@@ -461,8 +519,19 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
     if (nv > 0 && !wait_phase_bounded(b ? bar1 : bar0, static_cast<uint32_t>((it >> 1) & 1),
                                       static_cast<uint64_t>(timeout_ns)))
       timed_out = true;
-    const uint8_t* sl = buf[b];
-    // pass 1: max and sum of exponentials over the staged slice
+    uint8_t* sl = buf[b];
+    const int yl = yl_next;
+    if (row + nclusters < N) yl_next = labels[row + nclusters];
+    const int yt = (yl != ignore_index && yl >= 0 && yl < V) ? yl : -1;  // target, or -1
+    // The target's element, when it lies in this slice, is read by one thread in
+    // both loops of pass 1: that thread keeps z_t, counts it in its maximum and
+    // sets it to -inf in the staged copy, so that no sum (and no branch in the
+    // loops) includes it; the gradient pass writes the target's entry itself.
+    const int vt = (yt >= v0 * E && yt < v1 * E) ? yt / E - v0 : -1;  // its vector in the slice
+    const bool own = vt >= 0 && vt % kCeThreads == tid;
+    uint8_t* const tgt = sl + (own ? static_cast<int64_t>(yt - v0 * E) * kElt : 0);
+    // pass 1: max (the target included) and sum of exponentials (the target's
+    // term left out) over the staged slice
     float m = -INFINITY, s = 0.f;
     if constexpr (kBf16) {
       // The thread's maximum first, two elements per packed compare (exact on
@@ -478,6 +547,11 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
       }
       pm0 = bf16x2_max(pm0, pm1);
       m = fmaxf(bf16_lo(pm0), bf16_hi(pm0));
+      if (own) {   // after the maximum, before the sum (this thread reads it in both)
+        const uint16_t bits = *reinterpret_cast<const uint16_t*>(tgt);
+        s_zt = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+        *reinterpret_cast<uint16_t*>(tgt) = 0xFF80u;   // -inf
+      }
       if (m != -INFINITY) {
         const float ms = m * kLog2e;
         float acc0 = 0.f, acc1 = 0.f;
@@ -492,6 +566,11 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
         s = acc0 + acc1;
       }
     } else {
+      if (own) {   // before the online loop: its maximum starts at z_t
+        m = *reinterpret_cast<const float*>(tgt);
+        s_zt = m;
+        *reinterpret_cast<float*>(tgt) = -INFINITY;
+      }
       constexpr int kU = 2;
       int v = tid;
       for (; v + (kU - 1) * kCeThreads < nv; v += kU * kCeThreads) {
@@ -538,7 +617,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
     if (last) {
       for (int i = nvec * E + tid; i < V; i += kCeThreads) {
         const float x = VT::load1(zr + static_cast<int64_t>(i) * kElt);
-        lse_merge(m, s, x, 1.f);
+        lse_merge(m, s, x, i == yt ? 0.f : 1.f);
       }
     }
 #pragma unroll
@@ -549,6 +628,7 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
     }
     if (lane == 0) s_red[warp] = make_float2(m, s);
     __syncthreads();
+    RowStat rs;
     if (warp == 0) {
       float2 r = lane < kCeThreads / 32 ? s_red[lane] : make_float2(-INFINITY, 0.f);
       m = r.x;
@@ -560,15 +640,13 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
         lse_merge(m, s, m2, s2);
       }
       if (lane == 0) {  // tid 0: send this CTA's part of the row to every CTA
-        const int y = labels[row];
-        const bool valid = y != ignore_index && y >= 0 && y < V;
+        const int y = yt;
+        const bool valid = yt >= 0;
         // the target logit, from this CTA's staged slice (or its global tail),
         // so that no CTA reads a part of the row a peer may be overwriting
         float zt = 0.f;
-        if (valid && y >= v0 * E && y < v1 * E)
-          zt = kBf16 ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(
-                           sl + static_cast<int64_t>(y - v0 * E) * 2)) << 16)
-                     : *reinterpret_cast<const float*>(sl + static_cast<int64_t>(y - v0 * E) * 4);
+        if (vt >= 0)
+          zt = s_zt;   // written by its owner before the block barrier above
         else if (valid && last && y >= nvec * E)
           zt = VT::load1(zr + static_cast<int64_t>(y) * kElt);
         const int k = it & 1;
@@ -588,40 +666,55 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
           lse_merge(M, S, pr.x, pr.y);
           ZT += pr.z;
         }
-        const float lse = M + logf(S);
-        if (crank == 0) {
-          if (lse_out != nullptr) lse_out[row] = lse;
-          nll_out[row] = valid ? lse - ZT : 0.f;
+        rs = row_grad(M, S, ZT, valid, scale);
+        s_nm2 = -M * kLog2e;
+        if constexpr (kBf16) {
+          float lg;   // log2 |a|; -inf for a = 0 (an ignored token)
+          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(fabsf(rs.a)));
+          s_c = s_nm2 + lg;
         }
-        s_lse = lse;
-        s_y = valid ? y : -1;
+        s_a = rs.a;
+        s_q = rs.q;
+        s_y = yt;
       }
     }
     __syncthreads();
+    if (tid == 0 && crank == 0) {  // the loss, off the gradient pass's critical path
+      float lse, nll;
+      row_loss(rs, lse, nll);
+      if (lse_out != nullptr) lse_out[row] = lse;
+      nll_out[row] = nll;
+    }
     if constexpr (kGrad) {
-      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale from the staged slice
-      const float lse = s_lse;
+      // pass 2: dZ = (exp(z - lse) - [v = y]) * scale from the staged slice, as
+      // exp(z - M) * a off the target (a = scale / S) and -scale * (1 - p) at it.
+      // Off the target the exponent is one FMA, with log2 |a| folded in for bf16
+      // rows and a's sign applied to the packed pair: the rounding of those row
+      // constants is a common relative error of about 1e-6 per entry, and the
+      // target's entry, where a difference would lose it, does not use them.
+      const float nm2 = s_nm2, a = s_a;
       const int y = s_y;
-      const float sc = y >= 0 ? scale : 0.f;
+      const float gt = y >= 0 ? -scale * s_q : 0.f;
       uint8_t* gr = g + static_cast<int64_t>(row) * gld_bytes;
-      // exponent (z - lse) * log2 e, the difference first: exact when z is close to
-      // lse, so a confident target keeps p - 1 to about an fp32 ulp
       if constexpr (kBf16) {
+        const float c = s_c;
+        const uint32_t sgn = a < 0.f ? 0x80008000u : 0u;
+        const float gt_pre = sgn ? -gt : gt;   // the pair's sign flip restores it
         for (int v = tid; v < nv; v += kCeThreads) {
           const uint4 w = *reinterpret_cast<const uint4*>(sl + static_cast<int64_t>(v) * 16);
           float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                         bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
+          for (int e = 0; e < 8; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, c));
           const int base = (v0 + v) * 8;
           if (static_cast<unsigned>(y - base) < 8u) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              if (base + e == y) x[e] -= sc;
+              if (base + e == y) x[e] = gt_pre;
           }
           *reinterpret_cast<uint4*>(gr + static_cast<int64_t>(v0 + v) * 16) =
-              make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                         pack_bf16(x[6], x[7]));
+              make_uint4(pack_bf16(x[0], x[1]) ^ sgn, pack_bf16(x[2], x[3]) ^ sgn,
+                         pack_bf16(x[4], x[5]) ^ sgn, pack_bf16(x[6], x[7]) ^ sgn);
         }
       } else {
         for (int v = tid; v < nv; v += kCeThreads) {
@@ -629,25 +722,25 @@ __global__ void __launch_bounds__(kCeThreads, kMinB)
           float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                         __uint_as_float(w.w)};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = ex2a((x[e] - lse) * kLog2e) * sc;
+          for (int e = 0; e < 4; ++e) x[e] = ex2a(fmaf(x[e], kLog2e, nm2)) * a;
           const int base = (v0 + v) * 4;
           if (static_cast<unsigned>(y - base) < 4u) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (base + e == y) x[e] -= sc;
+              if (base + e == y) x[e] = gt;
           }
           VT::store(gr + static_cast<int64_t>(v0 + v) * 16, x);
         }
       }
       if (last) {
         for (int i = nvec * E + tid; i < V; i += kCeThreads) {
-          float x = ex2a((VT::load1(zr + static_cast<int64_t>(i) * kElt) - lse) * kLog2e) * sc;
-          if (i == y) x -= sc;
+          float x = ex2a(fmaf(VT::load1(zr + static_cast<int64_t>(i) * kElt), kLog2e, nm2)) * a;
+          if (i == y) x = gt;
           VT::store1(gr + static_cast<int64_t>(i) * kElt, x);
         }
       }
     }
-    __syncthreads();  // the buffer, s_red, s_lse, s_y are reused
+    __syncthreads();  // the buffer, s_red and the row's values in shared memory are reused
   }
   if (timed_out && status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, 9);
   cluster_barrier();

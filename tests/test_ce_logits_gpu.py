@@ -120,6 +120,39 @@ def test_staged_rows_with_scales_and_ignored_tokens(bf16, grad_scale):
     assert torch.count_nonzero(res.dlogits[ignored]).item() == 0
 
 
+@pytest.mark.parametrize("N,V,bf16", [(64, 5003, False), (64, 40000, False), (48, 65600, True)])
+def test_confident_targets_keep_their_small_gradient(N, V, bf16):
+    """Logits with a standard deviation of 20 and half of the labels on the row's
+    largest logit, so p of those targets is close to 1: the gradient at the
+    target, scale * (p - 1), and the per-token loss, -log p, are small numbers
+    that a difference with the fp32 lse would lose. Both must match the oracle
+    to the output's own precision (1e-4 relative for fp32, one bf16 rounding for
+    bf16), on the streamed kernel (20 KB rows) and the staged one."""
+    ld = (V + 7) // 8 * 8
+    Z, y, t, lab = _logits(N, V, seed=48 + V % 7, std=20.0, ld=ld, bf16=bf16, p_ignore=0.1)
+    top = np.argmax(Z, axis=1).astype(np.int32)
+    half = np.arange(N) % 2 == 0
+    y = np.where((y != -100) & half, top, y).astype(np.int32)
+    lab = torch.from_numpy(y).to(t.device)
+    ref = oracle.ce_logits(Z, y)
+    res = flce.ce_logits(t, lab)
+    assert flce.check_status(res.status) == flce.FLCE_OK
+    _check(res, ref, y=y)
+    rows = np.nonzero(y != -100)[0]
+    g = tensor_to_f64(res.dlogits)[rows, y[rows]]
+    c = ref["dZ"][rows, y[rows]]
+    rel = (2.0 ** -8) if bf16 else 1e-4
+    # the float64 reference itself forms p - 1 with a cancellation: below 1e-12 of
+    # the scale its own rounding takes over (a difference with the fp32 lse would
+    # be off by about 1e-6 of the scale)
+    floor = 1e-12 * abs(float(grad_scale_f32(ref["n_valid"])))
+    assert np.all(np.abs(g - c) <= rel * np.abs(c) + floor), float(np.max(np.abs(g - c) / np.abs(c)))
+    per = flce.ce_logits(t, lab, need_grad=False, reduction="none")
+    nll = per.loss.double().cpu().numpy()
+    want = ref["nll"]
+    assert np.all(np.abs(nll - want) <= 1e-4 * np.abs(want) + 1e-6)
+
+
 def test_per_token_losses_forward_only():
     Z, y, t, lab = _logits(150, 2048, seed=43, p_ignore=0.2)
     res = flce.ce_logits(t, lab, need_grad=False, reduction="none")
