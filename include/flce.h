@@ -241,7 +241,10 @@ int flce_forward_backward_fp8(const uint8_t* H8, const float* scale_h, const uin
  * flce_backward_shard takes that lse (fp32 [N], 4-byte aligned) and writes the
  * shard's part of the gradients, G_iv = (exp(z_iv - lse_i) - [v = y_i]) * scale
  * over the shard's ids (scale = grad_scale / n as in flce_forward_backward, n
- * counted from the labels, or the normalizer option):
+ * counted from the labels, or the normalizer option). Having only lse, it forms
+ * the target entry as p * scale - scale, so for a token whose p is close to 1 that
+ * entry carries the fp32 rounding of lse (about 2^-24 |lse| of the scale), where
+ * flce_forward_backward, which keeps 1 - p from its own forward, does not:
  *   dH_part  fp32 [N, D], 16-byte aligned: G W_shard; the caller sums the parts of
  *            all shards (then rounds to bf16 if it wants bf16 dH); nullable
  *   dW_shard [V_shard, D], fp32 or bf16 (dw_dtype): the shard's rows of dW; nullable
