@@ -463,7 +463,7 @@ def other_workloads(args, flce, H, W, lab, wl_main, dev, local, stream, peaks) -
     entry that fails records its error instead of stopping the run."""
     import torch
     burst = peaks["bf16_tflops"]
-    steps, warmup = max(1, args.other_steps), 2
+    steps, warmup = max(1, args.other_steps), 3
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
     block = {"note": ("each entry timed in this run after the main measurement: seeded "
                       "inputs by the same recipe, default plan, CUDA events per step on the "
