@@ -86,6 +86,39 @@ def test_peaked_logits_at_the_stated_precision_pass():
     assert_within(errs)
 
 
+def test_target_entry_formed_from_the_fp32_lse_is_caught():
+    """The arithmetic the fused path had before forming 1 - p in its merge: G from
+    the fp32-rounded lse, the target entry as fl32(p * s) - s. On peaked logits
+    (lse about 145) that entry carries half an lse ulp of the scale, far beyond
+    itself for a confident token: the element-wise and per-row gates fail it."""
+    wl = flce_inputs.Workload("custom", 300, 256, 3000, 4.0, 0.5, "uniform", 0.05, seed=31)
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H = flce_inputs.bf16_bits_to_f64(Hb)
+    W = flce_inputs.bf16_bits_to_f64(Wb)
+    top = np.argmax(H @ W.T, axis=1).astype(np.int32)
+    half = np.arange(len(y)) % 2 == 0
+    y = np.where((y != -100) & half, top, y).astype(np.int32)
+    ref = oracle.flce(H, W, y, want_abs=True)
+    valid = y != -100
+    s = np.float32(1.0 / valid.sum())
+    lse32 = ref["lse"].astype(np.float32).astype(np.float64)
+    G = (np.exp(H @ W.T - lse32[:, None]).astype(np.float32) * s).astype(np.float32)
+    rows = np.nonzero(valid)[0]
+    G[rows, y[rows]] = (G[rows, y[rows]] - s).astype(np.float32)
+    G[~valid] = 0.0
+    Gb = _bf16(G)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    res = types.SimpleNamespace(loss=t(np.array([ref["loss"]], dtype=np.float32)),
+                                lse=t(ref["lse"].astype(np.float32)),
+                                dH=t(_bf16((Gb @ W).astype(np.float32)).astype(np.float32)).to(torch.bfloat16),
+                                dW=t((Gb.T @ H).astype(np.float32).astype(np.float64)))
+    errs = _errs(H, W, y, ref, res)
+    assert errs["dH_elem"] > 1.0 and errs["dW_elem"] > 1.0
+    assert errs["dH_soft_row"] > 1.0 and errs["dW_soft_row"] > 1.0
+    with pytest.raises(AssertionError):
+        assert_within(errs)
+
+
 def test_softmax_part_twenty_percent_off_is_caught():
     H, W, y, ref = _case()
     errs = _errs(H, W, y, ref, _host_result(H, W, y, ref, softmax_factor=0.8))
