@@ -157,6 +157,10 @@ int flce_get_plan(int64_t N, int64_t D, int64_t V, const flce_options* opt, int3
  * and dL/dW = (dL/dz)^T H), with the 1/N mean of the page's Python simulation
  * and the argument layout of the GPU MODE lecture 28 notes, cross-entropy
  * section (hidden states (B*S, hidden), LM-head weight (vocab, hidden), labels).
+ * The recompute takes the forward's per-token row maximum, sum of exponentials
+ * and 1 - p of the target (the pieces of the log-sum-exp, kept in the workspace),
+ * so that a confident token's gradient entry -scale * (1 - p) keeps fp32
+ * precision.
  *   H       bf16 [N, D]   hidden states (input)
  *   W       bf16 [V, D]   LM-head weight (input)
  *   labels  int32 [N]     target ids in [0, V) or ignore_index (input)
