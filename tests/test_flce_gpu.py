@@ -217,6 +217,25 @@ def test_run_to_run_bitwise_determinism():
     assert torch.equal(a.dW, b.dW)
 
 
+def test_full_size_bitwise_determinism():
+    """The long-sequence head (32768 tokens: 4 token blocks x 8 vocabulary chunks,
+    so dW is reduce-added across blocks and dH across chunks, each in launch
+    order, by the merged dH + dW launches of 760 units on every SM) gives the same
+    bits twice; the second call runs in a workspace left dirty by the first."""
+    wl = flce_inputs.get("long_seq")
+    Hb, Wb, y = flce_inputs.make_inputs(wl)
+    H, W, lab = to_device(Hb, Wb, y)
+    del Hb, Wb
+    ws = torch.empty(flce.workspace_size(wl.N, wl.D, wl.V), dtype=torch.uint8, device=H.device)
+    a = flce.forward_backward(H, W, lab, workspace=ws)
+    b = flce.forward_backward(H, W, lab, workspace=ws)
+    torch.cuda.synchronize()
+    assert flce.check_status(a.status) == flce.FLCE_OK and flce.check_status(b.status) == flce.FLCE_OK
+    assert torch.equal(a.loss, b.loss) and torch.equal(a.lse, b.lse)
+    assert torch.equal(a.dH.view(torch.int16), b.dH.view(torch.int16))
+    assert torch.equal(a.dW.view(torch.int32), b.dW.view(torch.int32))
+
+
 def test_optional_outputs_and_forward_only():
     Hb, Wb, y = _inputs(300, 128, 900, seed=16, p_ignore=0.1)
     H, W, lab = to_device(Hb, Wb, y)
