@@ -566,7 +566,23 @@ def other_workloads(args, flce, H, W, lab, wl_main, dev, local, stream, peaks) -
     return block
 
 
-def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -> dict:
+def small_pass_bytes(N, D, plan) -> dict:
+    """Algorithmic HBM bytes per step of the passes around the GEMMs (one read of
+    what each reads, one write of what each writes): the merge reads the
+    (max, sum) partials of every vocabulary range plus the target logits and the
+    labels and writes lse, the NLL and the per-token (max, 1 / sum, 1 - p, 0) of
+    the backward; the loss reduction reads the NLL and the labels; the rounding of
+    the fp32 dH accumulator (several chunks only) reads it and writes bf16 dH."""
+    npad = -(-N // 256) * 256
+    out = {"lse_merge": 8 * plan["v_splits"] * npad + 8 * N + 24 * N,
+           "loss_reduce": 8 * N}
+    if plan["n_chunks"] > 1:
+        out["dh_round"] = 6 * N * D
+    return out
+
+
+def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic,
+                  hbm_bytes_per_step=None) -> dict:
     """The roofline block of the JSON line from the per-kernel CUDA-event times.
 
     kernel_ms: ms per step of each kernel kind; n_kind / per_kind: launches and
@@ -576,7 +592,9 @@ def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -
     the largest time share. The kernels are timed as launches inside a step well
     under a second long, so the burst cuBLAS peak is the denominator; the
     sustained one is reported beside it. Every fraction is a quotient of the
-    block's own numbers and the peaks."""
+    block's own numbers and the peaks. hbm_bytes_per_step (small_pass_bytes) adds
+    to the HBM-bound passes their algorithmic GB/s and its fraction of the
+    measured copy bandwidth."""
     burst = peaks["bf16_tflops"]
     sustained = peaks.get("bf16_tflops_sustained", burst)
     gemm_flops = 2.0 * N * V * D   # per step, for each of the four products
@@ -594,6 +612,18 @@ def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -
         products[name] = {"kernel": k, "tflops": r, "frac": r / burst,
                           "frac_of_sustained": r / sustained}
     total = sum(kernel_ms.values())
+    kernels = {k: {"ms_per_step": kernel_ms[k],
+                   "ms_per_launch": per_kind[k] / max(n_kind[k], 1),
+                   "launches_per_step": n_kind[k] // steps,
+                   "tflops": mult.get(k, 1.0) * rate(kernel_ms[k]) if k.endswith("gemm") else None,
+                   "share": kernel_ms[k] / total}
+               for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dwdh_gemm",
+                         "dh_round"] if k in kernel_ms}
+    for k, nbytes in (hbm_bytes_per_step or {}).items():
+        if k in kernels and kernels[k]["ms_per_step"] > 0:
+            gbs = nbytes / (kernels[k]["ms_per_step"] / 1e3) / 1e9
+            kernels[k].update({"bound": "hbm", "algorithmic_bytes_per_step": nbytes, "gbs": gbs,
+                               "frac_of_hbm": gbs / peaks["hbm_gbs"]})
     return {
         "bound": "tensor", "unit": "TFLOP/s",
         "kernel": "flce_gemm_kernel<EPI_F32> (tcgen05, 256 x 512 tiles: dW = G^T H and dH = G W, one launch per chunk)",
@@ -608,13 +638,7 @@ def make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, traffic) -
         "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
                           "dram__bytes_write.sum per launch; null if the kernel changed)",
         "kernel_sha": kernel_source_sha(),
-        "kernels": {k: {"ms_per_step": kernel_ms[k],
-                        "ms_per_launch": per_kind[k] / max(n_kind[k], 1),
-                        "launches_per_step": n_kind[k] // steps,
-                        "tflops": mult.get(k, 1.0) * rate(kernel_ms[k]) if k.endswith("gemm") else None,
-                        "share": kernel_ms[k] / total}
-                    for k in ["lse_gemm", "lse_merge", "loss_reduce", "grad_gemm", "dwdh_gemm",
-                              "dh_round"] if k in kernel_ms},
+        "kernels": kernels,
     }
 
 
@@ -885,7 +909,8 @@ def main(argv=None) -> int:
     sustained = peaks.get("bf16_tflops_sustained", burst)
     roofline = make_roofline(N, V, D, kernel_ms, n_kind, per_kind, args.steps, peaks,
                              measured_traffic("flce_gemm_kernel<EPI_F32>", wl.name,
-                                              plan["v_chunk"]))
+                                              plan["v_chunk"]),
+                             hbm_bytes_per_step=small_pass_bytes(N, D, plan))
     products = roofline["products"]
     clocks = clk.summary()
 

@@ -58,3 +58,27 @@ def test_traffic_record_matches_only_its_kernel_sources_and_plan():
         assert bench.measured_traffic(r["kernel"], r["workload"], r["v_chunk"]) == r["bytes_per_launch"]
         assert bench.measured_traffic(r["kernel"], r["workload"], r["v_chunk"] + 256) is None
     assert bench.measured_traffic("flce_gemm_kernel<EPI_F32>", "no_such_workload", 16128) is None
+
+
+def test_hbm_passes_report_algorithmic_bandwidth():
+    """The passes around the GEMMs carry their algorithmic bytes (one read of what
+    each reads, one write of what each writes) and GB/s = bytes / time, as a
+    fraction of the measured copy bandwidth; the dH rounding only when there are
+    several chunks."""
+    N, V, D = 8192, 128256, 4096
+    peaks = bench.load_peaks()
+    kernel_ms, n_kind, per_kind, steps = _synthetic()
+    plan = {"v_splits": 101, "n_chunks": 8, "n_block": N}
+    nbytes = bench.small_pass_bytes(N, D, plan)
+    assert nbytes["dh_round"] == 6 * N * D                      # fp32 read + bf16 write
+    assert nbytes["loss_reduce"] == 8 * N                       # NLL + labels
+    assert nbytes["lse_merge"] == 8 * 101 * N + 32 * N          # partials + zt, labels + 3 outputs
+    r = bench.make_roofline(N, V, D, kernel_ms, n_kind, per_kind, steps, peaks, None,
+                            hbm_bytes_per_step=nbytes)
+    for k in ("lse_merge", "loss_reduce", "dh_round"):
+        kk = r["kernels"][k]
+        assert kk["bound"] == "hbm"
+        assert kk["gbs"] == pytest.approx(nbytes[k] / (kernel_ms[k] / 1e3) / 1e9, rel=1e-12)
+        assert kk["frac_of_hbm"] == pytest.approx(kk["gbs"] / peaks["hbm_gbs"], rel=1e-12)
+    assert "gbs" not in r["kernels"]["lse_gemm"]
+    assert "dh_round" not in bench.small_pass_bytes(N, D, dict(plan, n_chunks=1))
